@@ -1,0 +1,140 @@
+"""CPU oracle for verify attention (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package.  The C source ``verify_attn_oracle.c`` is the
+plain fp64 definition of the verify step's causal GQA attention over a paged,
+quantised KV cache; this module compiles it with gcc and marshals numpy arrays
+into it.  It shares no code with the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "verify_attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "int8": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        common = [P, P, P, P, P, P, I, P, I, I, I, I, I, I]
+        lib.oracle_verify_attn.argtypes = common + [P, P, I]
+        lib.oracle_verify_attn.restype = I
+        lib.oracle_verify_attn_rows.argtypes = common + [P, I, P, P, I]
+        lib.oracle_verify_attn_rows.restype = I
+        lib.oracle_verify_attn_partial.argtypes = common + [I, I, I, I, I, P, P]
+        lib.oracle_verify_attn_partial.restype = I
+        lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_bf16.restype = ctypes.c_double
+        lib.oracle_max_threads.argtypes = [I]
+        lib.oracle_max_threads.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _common(w):
+    """Argument tuple shared by every entry point, from a workload dict."""
+    dt = w["kv_dtype"]
+    raw = np.uint16 if dt == "bf16" else (np.uint8 if dt == "fp8_e4m3" else np.int8)
+    q = _c(w["q"], np.uint16)
+    k = _c(w["k_pages"], raw)
+    v = _c(w["v_pages"], raw)
+    ks = _c(w.get("k_scale"), np.float32)
+    vs = _c(w.get("v_scale"), np.float32)
+    bt = _c(w["block_table"], np.int32)
+    sl = _c(w["seq_lens"], np.int32)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    keep = (q, k, v, ks, vs, bt, sl)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
+            _ptr(sl), B, T, Hq, Hkv, D, KV_DTYPES[dt]]
+    return keep, args, (B, T, Hq, D)
+
+
+def verify_attn(w, nthreads: int = 0):
+    """Full oracle output: (out float64 [B,T,Hq,D], lse float64 [B,T,Hq])."""
+    lib = _load()
+    keep, args, (B, T, Hq, D) = _common(w)
+    out = np.empty((B, T, Hq, D), np.float64)
+    lse = np.empty((B, T, Hq), np.float64)
+    rc = lib.oracle_verify_attn(*args, _ptr(out), _ptr(lse), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_verify_attn rejected its arguments")
+    del keep
+    return out, lse
+
+
+def verify_attn_rows(w, rows, nthreads: int = 0):
+    """Oracle output for selected (b, t, h) triples: (out [n, D], lse [n])."""
+    lib = _load()
+    keep, args, (B, T, Hq, D) = _common(w)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.empty((n, D), np.float64)
+    lse = np.empty((n,), np.float64)
+    rc = lib.oracle_verify_attn_rows(*args, _ptr(rows), n, _ptr(out), _ptr(lse), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_verify_attn_rows rejected its arguments")
+    del keep
+    return out, lse
+
+
+def verify_attn_partial(w, b, t, h, key_begin, key_end):
+    """One split's normalised partial (out [D], lse) over keys [key_begin, key_end)."""
+    lib = _load()
+    keep, args, (B, T, Hq, D) = _common(w)
+    out = np.empty((D,), np.float64)
+    lse = np.empty((1,), np.float64)
+    rc = lib.oracle_verify_attn_partial(*args, b, t, h, key_begin, key_end, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_verify_attn_partial rejected its arguments")
+    del keep
+    return out, float(lse[0])
+
+
+def decode_e4m3(code: int) -> float:
+    return _load().oracle_decode_e4m3(code)
+
+
+def decode_bf16(bits: int) -> float:
+    return _load().oracle_decode_bf16(bits)
+
+
+def max_threads(nthreads: int = 0) -> int:
+    return _load().oracle_max_threads(nthreads)

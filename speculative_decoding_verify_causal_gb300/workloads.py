@@ -1,0 +1,233 @@
+"""Seeded synthetic workloads for verify attention.
+
+This module only *makes inputs*: random numbers, rounding to the stored
+formats, page shuffling and the planted needles / peaks.  It holds none of the
+attention arithmetic, so the CUDA path and the CPU oracle can both be fed from
+it without sharing any of the method's code.
+
+Input recipe (the same for tests, smoke check and benchmark):
+
+* RNG: ``numpy.random.Generator(PCG64(seed))``; the named configs use
+  ``seed = 20260 + index``.
+* q, k, v ~ N(0, 1) in fp32, rounded to bf16 (round-to-nearest-even).
+* Quantised caches store one fp32 scale per (token, kv-head):
+  ``a = max |x|`` over head_dim; fp8-e4m3 uses ``s = a / 448`` and stores
+  ``e4m3(x / s)`` (round-to-nearest-even, clamped to +-448); int8 uses
+  ``s = a / 127`` and stores ``clamp(rint(x / s), -127, 127)``; ``a == 0``
+  gives ``s = 1``.
+* Paged cache: 16-token pages, page ids shuffled by the seed; a batch draws its
+  pages from one shared pool assigned in order after the shuffle; slots past
+  the end of a sequence are zero.
+* Needles: key ``20 * qhat`` with ``qhat`` the unit vector of query 0 (first
+  q-head of the kv-head's group, verify token 0), planted before quantisation.
+* Peaks: a seeded 1 % of (token, kv-head) key rows multiplied by 4 before
+  quantisation.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+PAGE = 16
+KV_ELEM_BYTES = {"bf16": 2, "fp8_e4m3": 1, "int8": 1}
+_CHUNK_TOKENS = 8192  # fixed draw granularity: keeps the stream reproducible
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    name: str
+    index: int
+    seq_lens: tuple  # context lengths before adding T (one per sequence), or None
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    kv_dtype: str
+    needles: str = ""  # "random3" | "depths" | ""
+    peaks: float = 0.0
+    batch: int = 1
+    ctx_range: tuple = ()  # (lo, hi) uniform context lengths for a batch
+
+    @property
+    def description(self):
+        return _DESCRIPTIONS[self.name]
+
+
+_DESCRIPTIONS = {
+    "tiny": "1 seq, 256+5 tokens, 4 q / 1 kv heads, D=64, bf16 KV",
+    "mtp4": "1 seq, 1536+5 tokens, 24 q / 4 kv heads, D=256, fp8-e4m3 KV, 3 needles per kv head",
+    "lookup16": "1 seq, 25000+16 tokens, 24 q / 4 kv heads, D=256, int8 KV, 1% keys x4",
+    "batched": "64 seqs, U[1000,8000]+5 tokens, 24 q / 4 kv heads, D=256, fp8-e4m3 KV, shared page pool",
+    "maxctx": "1 seq, 262144+16 tokens, 24 q / 4 kv heads, D=256, int8 KV, needles at 10/50/90/99%",
+}
+
+CONFIGS = {
+    "tiny": Config("tiny", 0, (256,), 5, 4, 1, 64, "bf16"),
+    "mtp4": Config("mtp4", 1, (1536,), 5, 24, 4, 256, "fp8_e4m3", needles="random3"),
+    "lookup16": Config("lookup16", 2, (25000,), 16, 24, 4, 256, "int8", peaks=0.01),
+    "batched": Config("batched", 3, None, 5, 24, 4, 256, "fp8_e4m3", batch=64, ctx_range=(1000, 8000)),
+    "maxctx": Config("maxctx", 4, (262144,), 16, 24, 4, 256, "int8", needles="depths"),
+}
+
+
+def _bf16_round(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 (RNE) -> fp32."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _quantise(x: np.ndarray, kv_dtype: str):
+    """Store rows x [..., D] (fp32) in the cache format: (raw, scale or None)."""
+    if kv_dtype == "bf16":
+        return _bf16_bits(x), None
+    a = np.max(np.abs(x), axis=-1).astype(np.float32)
+    qmax = np.float32(448.0 if kv_dtype == "fp8_e4m3" else 127.0)
+    s = np.where(a > 0, a / qmax, np.float32(1.0)).astype(np.float32)
+    y = (x / s[..., None]).astype(np.float32)
+    if kv_dtype == "fp8_e4m3":
+        y = np.clip(y, -448.0, 448.0)
+        raw = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    else:
+        raw = np.clip(np.rint(y), -127, 127).astype(np.int8)
+    return raw, s
+
+
+def _normal_rows(rng, n_tokens, Hkv, D):
+    out = np.empty((n_tokens, Hkv, D), np.float32)
+    for s in range(0, n_tokens, _CHUNK_TOKENS):
+        e = min(n_tokens, s + _CHUNK_TOKENS)
+        out[s:e] = rng.standard_normal((e - s, Hkv, D), dtype=np.float32)
+    return out
+
+
+def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peaks=0.0,
+                  extra_pages=0, bt_stride=None, name="custom"):
+    """Build one synthetic verify-attention problem.
+
+    ``seq_lens`` are the full lengths L_b (they include the T verify tokens).
+    ``needles``: None, or a callable ``(rng, b, L) -> list of token positions``
+    at which every kv head gets a needle key.  Returns a dict of host arrays.
+    """
+    seq_lens = [int(x) for x in seq_lens]
+    B = len(seq_lens)
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    rng = np.random.Generator(np.random.PCG64(seed))
+
+    q32 = _bf16_round(rng.standard_normal((B, T, Hq, D), dtype=np.float32))
+    pages_per_seq = [(L + PAGE - 1) // PAGE for L in seq_lens]
+    num_pages = sum(pages_per_seq) + int(extra_pages)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    stride = max(pages_per_seq) if bt_stride is None else int(bt_stride)
+    if stride < max(pages_per_seq):
+        raise ValueError("bt_stride too small")
+    block_table = np.zeros((B, stride), np.int32)
+    off = 0
+    for b, n in enumerate(pages_per_seq):
+        block_table[b, :n] = perm[off:off + n]
+        off += n
+
+    raw_dtype = np.uint16 if kv_dtype == "bf16" else (np.uint8 if kv_dtype == "fp8_e4m3" else np.int8)
+    k_pages = np.zeros((num_pages, PAGE, Hkv, D), raw_dtype)
+    v_pages = np.zeros((num_pages, PAGE, Hkv, D), raw_dtype)
+    quant = kv_dtype != "bf16"
+    k_scale = np.zeros((num_pages, PAGE, Hkv), np.float32) if quant else None
+    v_scale = np.zeros((num_pages, PAGE, Hkv), np.float32) if quant else None
+    needle_pos = []
+    k_flat = k_pages.reshape(num_pages * PAGE, Hkv, D)
+    v_flat = v_pages.reshape(num_pages * PAGE, Hkv, D)
+    for b, L in enumerate(seq_lens):
+        k = _bf16_round(_normal_rows(rng, L, Hkv, D))
+        v = _bf16_round(_normal_rows(rng, L, Hkv, D))
+        pos = []
+        if needles is not None:
+            pos = list(needles(rng, b, L))
+            for g in range(Hkv):
+                q0 = q32[b, 0, g * G].astype(np.float64)
+                qhat = (q0 / np.linalg.norm(q0)).astype(np.float32)
+                for j in pos:
+                    k[j, g] = np.float32(20.0) * qhat
+        needle_pos.append(pos)
+        if peaks > 0:
+            n_pk = int(round(peaks * L * Hkv))
+            pick = rng.choice(L * Hkv, size=n_pk, replace=False)
+            k.reshape(L * Hkv, D)[pick] *= np.float32(4.0)
+        tok = np.arange(L)
+        phys = block_table[b, tok // PAGE].astype(np.int64) * PAGE + tok % PAGE
+        kr, ks = _quantise(k, kv_dtype)
+        vr, vs = _quantise(v, kv_dtype)
+        k_flat[phys] = kr
+        v_flat[phys] = vr
+        if quant:
+            k_scale.reshape(-1, Hkv)[phys] = ks
+            v_scale.reshape(-1, Hkv)[phys] = vs
+        del k, v, kr, vr
+    return {
+        "name": name,
+        "seed": seed,
+        "q": _bf16_bits(q32),
+        "k_pages": k_pages,
+        "v_pages": v_pages,
+        "k_scale": k_scale,
+        "v_scale": v_scale,
+        "block_table": block_table,
+        "seq_lens": np.asarray(seq_lens, np.int32),
+        "T": T,
+        "Hq": Hq,
+        "Hkv": Hkv,
+        "D": D,
+        "kv_dtype": kv_dtype,
+        "num_pages": num_pages,
+        "needle_pos": needle_pos,
+    }
+
+
+def config_workload(name: str):
+    """One of the five named configurations, fully materialised."""
+    c = CONFIGS[name]
+    seed = 20260 + c.index
+    if c.batch > 1:
+        lens_rng = np.random.Generator(np.random.PCG64(seed + 1000))
+        ctx = lens_rng.integers(c.ctx_range[0], c.ctx_range[1] + 1, size=c.batch)
+        seq_lens = [int(x) + c.T for x in ctx]
+    else:
+        seq_lens = [x + c.T for x in c.seq_lens]
+    needles = None
+    if c.needles == "random3":
+        def needles(rng, b, L, T=c.T):
+            return sorted(int(x) for x in rng.choice(L - T, size=3, replace=False))
+    elif c.needles == "depths":
+        def needles(rng, b, L, ctx=c.seq_lens[0]):
+            return [int(math.floor(p * ctx)) for p in (0.10, 0.50, 0.90, 0.99)]
+    return make_workload(seed, seq_lens, c.T, c.Hq, c.Hkv, c.D, c.kv_dtype,
+                         needles=needles, peaks=c.peaks, name=name)
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one verify call must move at minimum: every live KV row of every
+    kv head (plus its two scales when quantised), q, out (bf16), lse (fp32),
+    the block-table entries in use and seq_lens.  Split partials excluded."""
+    Hkv, D, T, Hq = w["Hkv"], w["D"], w["T"], w["Hq"]
+    eb = KV_ELEM_BYTES[w["kv_dtype"]]
+    quant = w["kv_dtype"] != "bf16"
+    lens = np.asarray(w["seq_lens"], np.int64)
+    B = len(lens)
+    kv = int(lens.sum()) * Hkv * (2 * D * eb + (8 if quant else 0))
+    pages = int(((lens + PAGE - 1) // PAGE).sum())
+    return kv + 2 * (B * T * Hq * D * 2) + B * T * Hq * 4 + 4 * (pages + B)
+
+
+def algorithmic_flops(w) -> int:
+    """4*D flops per (visible key, query row): QK^T and PV multiply-adds."""
+    lens = np.asarray(w["seq_lens"], np.int64)
+    T, Hq, D = w["T"], w["Hq"], w["D"]
+    visible = sum(int(L) - T + t + 1 for L in lens for t in range(T))
+    return 4 * D * Hq * visible
