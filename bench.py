@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the verify-attention library on one GB300 (or N replicas).
+
+One step = one verify_attn call (the partial-attention kernel plus the
+log-sum-exp combine) over the whole workload, using a plan built once from
+the live sequence lengths (planning is host work shared by every attention
+layer of a verify pass; its cost is reported separately as plan_us).
+
+Default workload: the long lookup-augmented verify block (1 sequence, 25,000
+cached + 16 verify tokens, 24 q / 4 kv heads, head_dim 256, int8 KV with
+per-token scales).  The cache is smaller than L2, so the timed loop rotates
+through enough independent cache copies that every call reads its KV from
+HBM.  Steps are replayed from a CUDA graph so that launch overhead does not
+pace the GPU.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (the reference arm of this build: there is no other
+implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify_attn µs/call and effective HBM GB/s (% of GB300 peak) at T=16, 25k ctx"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="lookup16",
+                    help="tiny | mtp4 | lookup16 | batched | maxctx")
+    ap.add_argument("--path", default="auto", choices=["auto", "warp", "mma"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.5, help="seconds of replays for the clock record")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons at 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        busy = [s for s in sm]
+        return {
+            "sm_mhz": statistics.median(busy) if busy else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+            "power_w_max": max(power) if power else None,
+        }
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(w, wl, max_rows=None):
+    """Time the oracle as it stands on the host cores over a bounded sample:
+    the packed rows of kv head 0 of sequence 0 (or the first max_rows of them)."""
+    import oracle
+    G = w["Hq"] // w["Hkv"]
+    rows = [(0, t, h) for t in range(w["T"]) for h in range(G)]
+    if max_rows:
+        rows = rows[:max_rows]
+    cores = oracle.max_threads(0)
+    t0 = time.perf_counter()
+    oracle.verify_attn_rows(w, rows, nthreads=0)
+    dt = time.perf_counter() - t0
+    frac = len(rows) / (w["q"].shape[0] * w["T"] * w["Hq"])
+    byts = wl.algorithmic_bytes(w) * frac
+    return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of {w['q'].shape[0] * w['T'] * w['Hq']} (seq, token, q-head) rows "
+                      f"(kv head 0 of sequence 0), fp64, {dt:.2f} s",
+            "seconds": dt}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    from speculative_decoding_verify_causal_gb300 import workloads as wl
+    import oracle
+    w = wl.config_workload(args.config)
+    cores = oracle.max_threads(0)
+    B, T, Hq = w["q"].shape[:3]
+    all_rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
+    per_step = max(1, cores)
+    frac = per_step / len(all_rows)
+    step_bytes = wl.algorithmic_bytes(w) * frac
+    i = 0
+
+    def step():
+        nonlocal i
+        rows = [all_rows[(i + k) % len(all_rows)] for k in range(per_step)]
+        i += per_step
+        oracle.verify_attn_rows(w, rows, nthreads=0)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    ms = dt / args.steps * 1e3
+    value = step_bytes / (dt / args.steps) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {wl.CONFIGS[args.config].description}",
+                   "step": f"{per_step} of {len(all_rows)} query rows per step (fp64 oracle)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} query rows per step, cycling over all rows"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def traffic_record(kernel, config):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(kernel, {}).get(config)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "speculative_decoding_verify_causal_gb300", "csrc", ent["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except Exception:
+        return None
+    return ent["bytes_per_launch"] if h == ent.get("source_sha256_16") else None
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from speculative_decoding_verify_causal_gb300 import build as vbuild
+    vbuild.build()
+    import speculative_decoding_verify_causal_gb300 as va
+    from speculative_decoding_verify_causal_gb300 import workloads as wl
+
+    w = wl.config_workload(args.config)
+    nbytes = wl.algorithmic_bytes(w)
+    kv_bytes = nbytes - 2 * w["q"].size * 2
+    copies = 1 if kv_bytes > 4 * L2_BYTES else int(math.ceil(4 * L2_BYTES / kv_bytes))
+    d = wl.to_device(w, dev, copies=copies)
+    stream = torch.cuda.Stream(dev)
+
+    # plan (host) cost, then the plan used by the timed loop
+    plan_times = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        p = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=args.path)
+        plan_times.append((time.perf_counter() - t0) * 1e6)
+        p.destroy()
+    plan = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=args.path)
+    info = plan.info()
+    launches_per_step = 1 + (1 if info["num_split_groups"] > 0 else 0)
+
+    def call(i, s):
+        k, v, ks, vs = d["caches"][i % copies]
+        va.verify_attn_with_plan(plan, d["q"], k, v, ks, vs, d["block_table"], d["seq_lens"], w["T"],
+                                 d["out"], d["lse"], stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            call(i, stream)
+    torch.cuda.synchronize()
+
+    # capture one graph of `copies` calls (and one for the remainder), with an
+    # event pair around every partial-attention kernel
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(copies)]
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s = torch.cuda.current_stream()
+            for i in range(n):
+                if with_events:
+                    va.verify_attn_plan_set_events(plan, *ev_pairs[i])
+                call(i, s)
+            va.verify_attn_plan_set_events(plan, None, None)
+        return g
+
+    g_full = capture(copies, True)
+    rem = args.steps % copies
+    g_rem = capture(rem, False) if rem else None
+    replays = args.steps // copies
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(replays):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    partial_ms = None
+    if replays > 0:
+        try:
+            partial_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs)
+        except Exception:
+            partial_ms = None
+    # keep the GPU busy with the same graph so the clock record sees the load
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t0 < args.soak_s:
+            for _ in range(50):
+                g_full.replay()
+            torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * nbytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs copied in, the
+    # result copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for key in ("q", "k_pages", "v_pages", "k_scale", "v_scale", "block_table", "seq_lens"):
+            t = d[key]
+            host[key] = None if t is None else t.cpu().pin_memory()
+        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+        out_h = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+        lse_h = torch.empty(d["lse"].shape, dtype=d["lse"].dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            va.verify_attn_with_plan(plan, dev_in["q"], dev_in["k_pages"], dev_in["v_pages"], dev_in["k_scale"],
+                                     dev_in["v_scale"], dev_in["block_table"], dev_in["seq_lens"], w["T"],
+                                     d["out"], d["lse"], stream=stream)
+            out_h.copy_(d["out"], non_blocking=True)
+            lse_h.copy_(d["lse"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "us_per_call": e2e_ms * 1e3, "steps": n_e2e}
+
+    if rank != 0:
+        plan.destroy()
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_src = peaks()
+    kernel = "va_mma_partial" if info["path"] == 2 else "va_warp_partial"
+    roof = None
+    if partial_ms:
+        achieved = nbytes / (partial_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic_record(kernel, args.config), "kernel": kernel,
+                "kernel_us": partial_ms * 1e3, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": nbytes}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, wl)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16" if info["path"] == 2 else "f32", "data": "synthetic",
+        "us_per_call": ms_per_step * 1e3,
+        "frac_of_peak_hbm": value / world / peak,
+        "config": {
+            "workload": f"{args.config}: {wl.CONFIGS[args.config].description}",
+            "kv_dtype": w["kv_dtype"], "T": w["T"], "seq_lens_sum": int(w["seq_lens"].sum()),
+            "num_seqs": int(len(w["seq_lens"])), "Hq": w["Hq"], "Hkv": w["Hkv"], "head_dim": w["D"],
+            "algorithmic_bytes": nbytes,
+            "l2": (f"rotating {copies} cache copies ({copies * kv_bytes / 1e6:.0f} MB >= 4x L2)"
+                   if copies > 1 else "cache larger than 4x L2"),
+            "graph": "CUDA graph replay", "parallelism": f"replicas x{world}",
+            "plan": info, "plan_us": statistics.median(plan_times),
+        },
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    plan.destroy()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

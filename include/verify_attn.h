@@ -1,0 +1,193 @@
+/*
+ * verify_attn.h -- C ABI of the GB300 (sm_103a) verify-attention library.
+ *
+ * The operation.  Speculative decoding drafts a short block of T tokens and
+ * checks them with one forward pass of the target model ("I pushed
+ * Qwen3.8-27B to 124 tps on a single request on a RTX 3090", bullets "MTP-4
+ * drafts" -> T = 5 and "Split-KV attention kernel for the verify step";
+ * "I pushed Qwen3.8-27B to 381 tps for a single request on a RTX 3090",
+ * "Longer verify blocks" -> T = 16).  In every attention layer of that pass,
+ * the T verify queries attend causally to a long paged KV cache.  With G =
+ * num_q_heads / num_kv_heads query heads per kv head, the G*T query rows of
+ * one kv head share every key, so the library packs them into one tile and
+ * reads each KV byte once per kv head.  The cache length is split across the
+ * GPU's SMs ("split-KV") and the per-split partial results are merged by
+ * log-sum-exp, so that a handful of queries still fill the chip (the same
+ * bullet: FlashAttention-2 split KV only for one query and left most SMs
+ * idle).  The split geometry is chosen from the live context lengths only,
+ * never from a declared maximum ("Four Tesla V100s from 2017 matched my RTX
+ * 5090 on single-request Qwen 3.8 decode", sections "This is a server, not a
+ * GEMM screenshot" and "What about long context?": a declared max context
+ * that leaked into the partition geometry taxed short requests).
+ *
+ * Definition (exact up to rounding), for sequence b with L_b cached tokens
+ * (L_b includes the T verify tokens), verify token t, query head h and kv
+ * head g = h / G:
+ *     Khat[j] = decode(k_pages[block_table[b][j/16], j%16, g, :]) * k_scale[...]
+ *     s_j     = (1/sqrt(head_dim)) * <q[b,t,h,:], Khat[j]>,  j <= L_b - T + t
+ *     lse     = ln sum_j exp(s_j)
+ *     out     = sum_j exp(s_j - lse) * Vhat[j]
+ * bf16 caches use scale 1 (scale pointers may be NULL).
+ *
+ * Memory layouts (row-major, contiguous, all on the device unless noted):
+ *     q            bf16  [B, T, Hq, D]
+ *     k_pages      [num_pages, 16, Hkv, D] of bf16 / fp8-e4m3 / int8
+ *     v_pages      same layout as k_pages
+ *     k_scale      fp32  [num_pages, 16, Hkv]   (one scale per token, kv head)
+ *     v_scale      fp32  [num_pages, 16, Hkv]
+ *     block_table  int32 [B, block_table_stride]  physical page of each
+ *                  16-token logical block; stride defaults to
+ *                  max_b ceil(L_b / 16)
+ *     seq_lens     int32 [B]   same values as given to the planner
+ *     out          bf16  [B, T, Hq, D]
+ *     lse          fp32  [B, T, Hq]   natural-log log-sum-exp of the scaled
+ *                  scores (may be NULL when not wanted)
+ * Row r of a kv head's packed tile is verify token t = r / G, query head
+ * h = g*G + r % G.
+ *
+ * Ownership.  The caller owns every tensor and the stream.  A plan owns its
+ * device work list and split-partial workspace and frees them in
+ * verify_attn_plan_destroy.  Calls on one plan share that workspace, so they
+ * must be ordered on one stream (or otherwise serialised).
+ *
+ * Errors.  Every int-returning call returns VA_OK (0) or a negative va_status.
+ * Nothing throws across the ABI and nothing traps on the device.  Launches
+ * are asynchronous: a VA_OK from verify_attn means the work was enqueued.
+ * When the plan knows the page-pool size (va_plan_options.num_pages > 0) the
+ * kernels check every block-table entry; a bad entry is skipped (its keys
+ * read as absent) and recorded in a device flag word that
+ * verify_attn_plan_device_flags returns.  A device seq_lens value that
+ * differs from the planned one is recorded the same way.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tokens per KV page (vLLM's default block size, kept for attention layers
+ * by "I pushed Qwen3.8-27B to 381 tps ...", "DFlash2 past 64k"). */
+#define VA_PAGE_SIZE 16
+
+typedef struct va_plan va_plan;
+
+typedef enum {
+    VA_BF16 = 0,     /* 2-byte bfloat16 cache, no scales */
+    VA_FP8_E4M3 = 1, /* OCP fp8 e4m3, fp32 scale per (token, kv head) */
+    VA_INT8 = 2      /* int8, fp32 scale per (token, kv head) */
+} va_kv_dtype;
+
+typedef enum {
+    VA_OK = 0,
+    VA_ERR_INVALID_ARGUMENT = -1, /* null pointer, T < 1, Hq % Hkv != 0, L_b < T ... */
+    VA_ERR_UNSUPPORTED = -2,      /* head_dim not in {64, 128, 256}, unknown dtype */
+    VA_ERR_PLAN_MISMATCH = -3,    /* call arguments disagree with the plan */
+    VA_ERR_NO_PLAN = -4,          /* verify_attn with no current plan on this thread */
+    VA_ERR_CUDA = -5,             /* a CUDA runtime call or launch failed */
+    VA_ERR_OUT_OF_MEMORY = -6,    /* workspace allocation failed */
+    VA_ERR_NO_DEVICE = -7         /* no usable CUDA device */
+} va_status;
+
+/* Which partial-attention kernel a plan uses. */
+typedef enum {
+    VA_PATH_AUTO = 0,  /* tensor cores once the packed rows fill an MMA tile */
+    VA_PATH_WARP = 1,  /* CUDA-core kernel: warp-shuffle reductions, any row count */
+    VA_PATH_MMA = 2    /* tcgen05 tensor-core kernel (TMEM accumulators) */
+} va_path;
+
+/* Optional planner settings; zero-initialise for defaults. */
+typedef struct {
+    int block_table_stride; /* entries per block_table row; 0 = max_b ceil(L_b/16) */
+    int tokens_per_split;   /* force the split length (rounded up to the kernel's
+                               key tile); 0 = chosen by the planner */
+    int path;               /* va_path */
+    int num_pages;          /* page-pool size for device bound checks; 0 = no checks */
+} va_plan_options;
+
+/* Read-only summary of a plan (host data). */
+typedef struct {
+    int num_seqs, T, num_q_heads, num_kv_heads, head_dim, kv_dtype;
+    int path;               /* the va_path actually used */
+    int rows_per_group;     /* packed rows per work item (<= G*T) */
+    int num_row_groups;     /* ceil(G*T / rows_per_group) */
+    int tokens_per_split;   /* split length chosen */
+    int num_items;          /* work items (CTAs of the partial kernel) */
+    int num_split_groups;   /* (seq, kv head, row group) triples merged by the combine */
+    int max_splits;         /* largest split count of any sequence */
+    int num_sms;            /* SM count the plan was sized for */
+    long long workspace_bytes;
+} va_plan_info;
+
+/* Build a plan for one batch shape.  Host only: reads seq_lens_host
+ * (length num_seqs), chooses the split geometry from the live lengths and
+ * num_sms (0 = query the current device), uploads the work list and
+ * allocates the partial workspace on the current device.  On success
+ * *out_plan owns that memory and becomes the calling thread's current plan
+ * (used by verify_attn). */
+int verify_attn_plan(const int32_t *seq_lens_host, int num_seqs, int T,
+                     int num_q_heads, int num_kv_heads, int head_dim,
+                     va_kv_dtype kv_dtype, int num_sms, va_plan **out_plan);
+
+/* Same, with options (opts may be NULL). */
+int verify_attn_plan_ex(const int32_t *seq_lens_host, int num_seqs, int T,
+                        int num_q_heads, int num_kv_heads, int head_dim,
+                        va_kv_dtype kv_dtype, int num_sms,
+                        const va_plan_options *opts, va_plan **out_plan);
+
+/* Verify attention with the calling thread's current plan (the one most
+ * recently built on this thread and not yet destroyed).  stream is a
+ * cudaStream_t (NULL = legacy default stream).  Asynchronous. */
+int verify_attn(const void *q, const void *k_pages, const void *v_pages,
+                const float *k_scale, const float *v_scale,
+                const int32_t *block_table, const int32_t *seq_lens, int T,
+                void *out, float *lse, void *stream);
+
+/* Verify attention with an explicit plan (preferred form). */
+int verify_attn_with_plan(const va_plan *plan, const void *q,
+                          const void *k_pages, const void *v_pages,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          int T, void *out, float *lse, void *stream);
+
+/* Free a plan's device memory (NULL is a no-op).  Clears the thread's
+ * current plan if it was this one.  The caller must make sure no call that
+ * uses the plan is still running on the device. */
+void verify_attn_plan_destroy(va_plan *plan);
+
+/* Static English text for a va_status code. */
+const char *verify_attn_status_string(int status);
+
+/* Copy a plan's summary into *info (host only). */
+int verify_attn_plan_get_info(const va_plan *plan, va_plan_info *info);
+
+/* Pure host planning (no CUDA call, usable without a GPU): fills *info and,
+ * when items != NULL, up to max_items work items as 5 ints each
+ * (seq, kv_head, row_group, key_begin, key_end), in launch order. */
+int verify_attn_plan_describe(const int32_t *seq_lens_host, int num_seqs, int T,
+                              int num_q_heads, int num_kv_heads, int head_dim,
+                              va_kv_dtype kv_dtype, int num_sms,
+                              const va_plan_options *opts, va_plan_info *info,
+                              int32_t *items, int max_items);
+
+/* Read (and if clear != 0, reset) the plan's device flag word: bit 0 = a
+ * block-table entry outside [0, num_pages) was skipped, bit 1 = a device
+ * seq_lens value differed from the planned one.  Synchronises the stream. */
+int verify_attn_plan_device_flags(const va_plan *plan, int clear, int *flags,
+                                  void *stream);
+
+/* Measurement hook.  When set (both non-NULL), every later call with this
+ * plan records ev_before just before its partial-attention kernel and
+ * ev_after just after it, on the call's stream, so that a caller can time
+ * the dominant kernel alone (cudaEventElapsedTime).  The events are
+ * cudaEvent_t handles owned by the caller; pass NULL, NULL to stop.  Works
+ * under CUDA-graph capture (the records become graph nodes). */
+int verify_attn_plan_set_events(va_plan *plan, void *ev_before, void *ev_after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

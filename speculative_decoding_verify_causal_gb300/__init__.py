@@ -1,0 +1,301 @@
+"""GB300-native speculative-decoding verify attention.
+
+Thin ctypes binding over ``libverify_attn.so`` (built in-tree by
+``speculative_decoding_verify_causal_gb300.build``).  The functions carry the
+C ABI's names and do argument marshalling only: every step of the attention
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  There is no CPU fallback: importing this package without the built
+library raises.
+
+Layouts (see ``include/verify_attn.h``):
+  q bf16 [B, T, Hq, D]; k_pages / v_pages [num_pages, 16, Hkv, D] of
+  bf16 / fp8-e4m3 (uint8 storage) / int8; k_scale / v_scale fp32
+  [num_pages, 16, Hkv]; block_table int32 [B, stride]; seq_lens int32 [B];
+  out bf16 [B, T, Hq, D]; lse fp32 [B, T, Hq].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libverify_attn.so")
+
+VA_BF16, VA_FP8_E4M3, VA_INT8 = 0, 1, 2
+KV_DTYPE_CODES = {"bf16": VA_BF16, "fp8_e4m3": VA_FP8_E4M3, "int8": VA_INT8}
+VA_PATH_AUTO, VA_PATH_WARP, VA_PATH_MMA = 0, 1, 2
+PATH_CODES = {"auto": VA_PATH_AUTO, "warp": VA_PATH_WARP, "mma": VA_PATH_MMA}
+PAGE_SIZE = 16
+
+STATUS_NAMES = {
+    0: "VA_OK", -1: "VA_ERR_INVALID_ARGUMENT", -2: "VA_ERR_UNSUPPORTED",
+    -3: "VA_ERR_PLAN_MISMATCH", -4: "VA_ERR_NO_PLAN", -5: "VA_ERR_CUDA",
+    -6: "VA_ERR_OUT_OF_MEMORY", -7: "VA_ERR_NO_DEVICE",
+}
+
+
+class VerifyAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({verify_attn_status_string(status)})")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("block_table_stride", ctypes.c_int), ("tokens_per_split", ctypes.c_int),
+                ("path", ctypes.c_int), ("num_pages", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_seqs", "T", "num_q_heads", "num_kv_heads", "head_dim", "kv_dtype", "path",
+        "rows_per_group", "num_row_groups", "tokens_per_split", "num_items",
+        "num_split_groups", "max_splits", "num_sms")] + [("workspace_bytes", ctypes.c_longlong)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is not built: run `python -m speculative_decoding_verify_causal_gb300.build` "
+                "(the package has no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.verify_attn_plan.argtypes = [P, I, I, I, I, I, I, I, ctypes.POINTER(P)]
+        lib.verify_attn_plan_ex.argtypes = [P, I, I, I, I, I, I, I, ctypes.POINTER(_Options), ctypes.POINTER(P)]
+        lib.verify_attn.argtypes = [P] * 7 + [I, P, P, P]
+        lib.verify_attn_with_plan.argtypes = [P] + [P] * 7 + [I, P, P, P]
+        lib.verify_attn_plan_destroy.argtypes = [P]
+        lib.verify_attn_plan_destroy.restype = None
+        lib.verify_attn_status_string.argtypes = [I]
+        lib.verify_attn_status_string.restype = ctypes.c_char_p
+        lib.verify_attn_plan_get_info.argtypes = [P, ctypes.POINTER(PlanInfo)]
+        lib.verify_attn_plan_describe.argtypes = [P, I, I, I, I, I, I, I, ctypes.POINTER(_Options),
+                                                  ctypes.POINTER(PlanInfo), P, I]
+        lib.verify_attn_plan_device_flags.argtypes = [P, I, ctypes.POINTER(I), P]
+        lib.verify_attn_plan_set_events.argtypes = [P, P, P]
+        lib.verify_attn_plan_set_events.restype = I
+        for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
+                  "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
+            getattr(lib, f).restype = I
+        _lib = lib
+        return lib
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def verify_attn_status_string(status: int) -> str:
+    return _load().verify_attn_status_string(int(status)).decode()
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise VerifyAttnError(rc, what)
+
+
+def _dtype_code(kv_dtype):
+    return KV_DTYPE_CODES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+
+
+def _options(block_table_stride=0, tokens_per_split=0, path="auto", num_pages=0):
+    return _Options(int(block_table_stride), int(tokens_per_split),
+                    PATH_CODES[path] if isinstance(path, str) else int(path), int(num_pages))
+
+
+def _host_lens(seq_lens):
+    try:
+        import torch
+        if isinstance(seq_lens, torch.Tensor):
+            seq_lens = seq_lens.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(-1))
+
+
+class Plan:
+    """Owning handle of a ``va_plan`` (freed on ``destroy()`` or collection)."""
+
+    def __init__(self, handle, seq_lens, T, kv_dtype):
+        self._h = ctypes.c_void_p(handle)
+        self.seq_lens = seq_lens
+        self.T = T
+        self.kv_dtype = kv_dtype
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> dict:
+        return verify_attn_plan_get_info(self)
+
+    def destroy(self):
+        if self._h and self._h.value:
+            _load().verify_attn_plan_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def verify_attn_plan(seq_lens, T, num_q_heads, num_kv_heads, head_dim, kv_dtype, num_sms=0,
+                     **options) -> Plan:
+    """Plan one batch shape from the host ``seq_lens`` (lengths include the T
+    verify tokens).  Keyword options: block_table_stride, tokens_per_split,
+    path ("auto" | "warp" | "mma"), num_pages (enables device bound checks).
+    The new plan also becomes this thread's current plan for ``verify_attn``."""
+    lib = _load()
+    lens = _host_lens(seq_lens)
+    out = ctypes.c_void_p()
+    opts = _options(**options)
+    rc = lib.verify_attn_plan_ex(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T), int(num_q_heads),
+                                 int(num_kv_heads), int(head_dim), _dtype_code(kv_dtype), int(num_sms),
+                                 ctypes.byref(opts), ctypes.byref(out))
+    _check(rc, "verify_attn_plan")
+    return Plan(out.value, lens, int(T), _dtype_code(kv_dtype))
+
+
+def verify_attn_plan_destroy(plan: Plan):
+    plan.destroy()
+
+
+def verify_attn_plan_get_info(plan: Plan) -> dict:
+    info = PlanInfo()
+    _check(_load().verify_attn_plan_get_info(plan.handle, ctypes.byref(info)), "verify_attn_plan_get_info")
+    return info.as_dict()
+
+
+def verify_attn_plan_describe(seq_lens, T, num_q_heads, num_kv_heads, head_dim, kv_dtype, num_sms,
+                              max_items=None, **options):
+    """Host-only planning (no GPU needed): (info dict, items int32 [n, 5])
+    with items = (seq, kv_head, row_group, key_begin, key_end)."""
+    lib = _load()
+    lens = _host_lens(seq_lens)
+    opts = _options(**options)
+    info = PlanInfo()
+    rc = lib.verify_attn_plan_describe(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T),
+                                       int(num_q_heads), int(num_kv_heads), int(head_dim),
+                                       _dtype_code(kv_dtype), int(num_sms), ctypes.byref(opts),
+                                       ctypes.byref(info), None, 0)
+    _check(rc, "verify_attn_plan_describe")
+    n = info.num_items if max_items is None else min(int(max_items), info.num_items)
+    items = np.zeros((max(n, 1), 5), np.int32)
+    rc = lib.verify_attn_plan_describe(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T),
+                                       int(num_q_heads), int(num_kv_heads), int(head_dim),
+                                       _dtype_code(kv_dtype), int(num_sms), ctypes.byref(opts),
+                                       ctypes.byref(info), items.ctypes.data_as(ctypes.c_void_p), n)
+    _check(rc, "verify_attn_plan_describe")
+    return info.as_dict(), items[:n]
+
+
+def _dev_ptr(t, name, dtypes, allow_none=False):
+    import torch
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _kv_dtypes(code):
+    import torch
+    if code == VA_BF16:
+        return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+    if code == VA_FP8_E4M3:
+        return (torch.uint8, torch.float8_e4m3fn)
+    return (torch.int8,)
+
+
+def _marshal(kv_code, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse, stream):
+    import torch
+    q16 = (torch.bfloat16, torch.int16)
+    kvd = _kv_dtypes(kv_code)
+    args = [
+        _dev_ptr(q, "q", q16),
+        _dev_ptr(k_pages, "k_pages", kvd),
+        _dev_ptr(v_pages, "v_pages", kvd),
+        _dev_ptr(k_scale, "k_scale", (torch.float32,), allow_none=kv_code == VA_BF16),
+        _dev_ptr(v_scale, "v_scale", (torch.float32,), allow_none=kv_code == VA_BF16),
+        _dev_ptr(block_table, "block_table", (torch.int32,)),
+        _dev_ptr(seq_lens, "seq_lens", (torch.int32,)),
+    ]
+    tail = [_dev_ptr(out, "out", q16), _dev_ptr(lse, "lse", (torch.float32,), allow_none=True)]
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return args, tail, s
+
+
+def verify_attn_with_plan(plan: Plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, T,
+                          out, lse=None, stream=None):
+    """Enqueue verify attention with an explicit plan on ``stream`` (default:
+    torch's current stream).  Writes ``out`` (and ``lse`` if given)."""
+    args, tail, s = _marshal(plan.kv_dtype, q, k_pages, v_pages, k_scale, v_scale, block_table,
+                             seq_lens, out, lse, stream)
+    _check(_load().verify_attn_with_plan(plan.handle, *args, int(T), *tail, s), "verify_attn_with_plan")
+
+
+def verify_attn(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, T, out, lse=None,
+                stream=None, kv_dtype=None):
+    """Enqueue verify attention with this thread's current plan.  ``kv_dtype``
+    only selects the accepted tensor dtypes for marshalling (inferred from
+    ``k_pages`` when omitted)."""
+    import torch
+    if kv_dtype is None:
+        kv_code = {torch.int8: VA_INT8, torch.uint8: VA_FP8_E4M3,
+                   torch.float8_e4m3fn: VA_FP8_E4M3}.get(k_pages.dtype, VA_BF16)
+    else:
+        kv_code = _dtype_code(kv_dtype)
+    args, tail, s = _marshal(kv_code, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,
+                             out, lse, stream)
+    _check(_load().verify_attn(*args, int(T), *tail, s), "verify_attn")
+
+
+def verify_attn_plan_device_flags(plan: Plan, clear=True, stream=None) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    flags = ctypes.c_int(0)
+    _check(_load().verify_attn_plan_device_flags(plan.handle, int(bool(clear)), ctypes.byref(flags),
+                                                 ctypes.c_void_p(stream.cuda_stream)),
+           "verify_attn_plan_device_flags")
+    return flags.value
+
+
+def verify_attn_plan_set_events(plan: Plan, ev_before=None, ev_after=None):
+    """Record two torch.cuda.Event objects around the partial-attention
+    kernel of every later call with ``plan`` (None, None stops)."""
+    b = ctypes.c_void_p(ev_before.cuda_event) if ev_before is not None else None
+    a = ctypes.c_void_p(ev_after.cuda_event) if ev_after is not None else None
+    _check(_load().verify_attn_plan_set_events(plan.handle, b, a), "verify_attn_plan_set_events")
+
+
+__all__ = [
+    "verify_attn_plan_set_events",
+    "verify_attn_plan", "verify_attn", "verify_attn_with_plan", "verify_attn_plan_destroy",
+    "verify_attn_status_string", "verify_attn_plan_get_info", "verify_attn_plan_describe",
+    "verify_attn_plan_device_flags", "Plan", "VerifyAttnError", "library", "LIB_PATH",
+]

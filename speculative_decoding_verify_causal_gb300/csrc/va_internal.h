@@ -1,0 +1,67 @@
+// Internal declarations shared by the library's translation units (never
+// installed; the public surface is include/verify_attn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "verify_attn.h"
+
+namespace va {
+
+// One CTA's work: the packed rows of row group `rg` of kv head `kvh` of
+// sequence `b`, over keys [k_begin, k_end).  `L` is the planned sequence
+// length; `part` is the partial slot to write, or -1 when this item covers the
+// whole sequence and writes the final output directly.
+struct Item {
+    int b, kvh, rg, k_begin, k_end, L, part, pad;
+};
+
+// One (sequence, kv head, row group) whose splits the combine merges.
+struct Group {
+    int b, kvh, rg, first_part, n, pad0, pad1, pad2;
+};
+
+enum : int { kFlagBadPage = 1, kFlagSeqLenMismatch = 2 };
+
+// Everything a partial-attention kernel needs, passed by value.
+struct PartialParams {
+    const uint16_t *q;          // bf16 [B, T, Hq, D]
+    const void *k_pages;        // [num_pages, 16, Hkv, D]
+    const void *v_pages;
+    const float *k_scale;       // [num_pages, 16, Hkv] or null (bf16)
+    const float *v_scale;
+    const int32_t *block_table; // [B, bt_stride]
+    const int32_t *seq_lens;    // [B]
+    uint16_t *out;              // bf16 [B, T, Hq, D]
+    float *lse;                 // [B, T, Hq] or null
+    const Item *items;
+    float *o_part;              // [num_parts, rows_per_group, D]
+    float *lse_part;            // [num_parts, rows_per_group]
+    int *flags;
+    int bt_stride, T, Hq, Hkv, G, R, rows_per_group, num_pages;
+    float sm_scale_log2;        // log2(e) / sqrt(D)
+};
+
+struct CombineParams {
+    const Group *groups;
+    const float *o_part;
+    const float *lse_part;
+    uint16_t *out;
+    float *lse;
+    int T, Hq, G, R, rows_per_group, D;
+};
+
+// Kernel launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_warp_partial(const PartialParams &p, int head_dim, int kv_dtype,
+                                int num_items, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, int num_groups, int max_splits,
+                           cudaStream_t s);
+
+// Geometry of each path.
+constexpr int kWarpRows = 16;    // packed rows per work item, CUDA-core kernel
+constexpr int kWarpTile = 32;    // keys per smem tile, CUDA-core kernel
+constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
+constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
+
+}  // namespace va

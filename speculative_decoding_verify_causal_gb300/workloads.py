@@ -231,3 +231,34 @@ def algorithmic_flops(w) -> int:
     T, Hq, D = w["T"], w["Hq"], w["D"]
     visible = sum(int(L) - T + t + 1 for L in lens for t in range(T))
     return 4 * D * Hq * visible
+
+
+def to_device(w, device="cuda", copies=1):
+    """Device tensors of a workload (torch).  ``copies`` > 1 makes that many
+    independent copies of the cache tensors (to rotate through, so that a
+    timing loop does not re-read the cache from L2)."""
+    dev = torch.device(device)
+
+    def t(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q = torch.from_numpy(np.ascontiguousarray(w["q"]).view(np.int16)).to(dev).view(torch.bfloat16)
+    kv_caches = []
+    for i in range(max(1, copies)):
+        if w["kv_dtype"] == "bf16":
+            k = torch.from_numpy(w["k_pages"].view(np.int16)).to(dev).view(torch.bfloat16)
+            v = torch.from_numpy(w["v_pages"].view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            k, v = t(w["k_pages"]), t(w["v_pages"])
+        kv_caches.append((k, v, t(w["k_scale"]), t(w["v_scale"])))
+    B, T, Hq, D = w["q"].shape
+    return {
+        "q": q,
+        "caches": kv_caches,
+        "k_pages": kv_caches[0][0], "v_pages": kv_caches[0][1],
+        "k_scale": kv_caches[0][2], "v_scale": kv_caches[0][3],
+        "block_table": t(w["block_table"]),
+        "seq_lens": t(w["seq_lens"]),
+        "out": torch.zeros((B, T, Hq, D), dtype=torch.bfloat16, device=dev),
+        "lse": torch.zeros((B, T, Hq), dtype=torch.float32, device=dev),
+    }

@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 CPU
+oracle, element by element, on the same seeded inputs.  Full outputs for the
+small cases; sampled (b, t, h) rows, computed one by one by the oracle, for
+the full-size configurations in the launch configuration the benchmark uses."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verify_causal_gb300 import workloads as wl
+
+from parity import compare, run_gpu
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from speculative_decoding_verify_causal_gb300 import build
+    build.build()
+
+
+_cache = {}
+
+
+def config(name):
+    if name not in _cache:
+        _cache[name] = wl.config_workload(name)
+    return _cache[name]
+
+
+# ------------------------------------------------------------ named configs
+@pytest.mark.parametrize("name", ["tiny", "mtp4"])
+@pytest.mark.parametrize("path", ["auto", "warp"])
+def test_small_configs_full_output(name, path):
+    w = config(name)
+    out, lse, info = run_gpu(w, {"path": path})
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"{name}/{path} {info}")
+
+
+def _sample_rows(w, n_extra=12, seed=0):
+    B, T, Hq = w["q"].shape[:3]
+    G = Hq // w["Hkv"]
+    rows = {(0, 0, 0), (B - 1, T - 1, Hq - 1), (0, T - 1, 0), (B - 1, 0, Hq - 1)}
+    for g in range(w["Hkv"]):  # needle-aligned heads (query 0 of each group)
+        rows.add((0, 0, g * G))
+    rng = np.random.default_rng(seed)
+    for _ in range(n_extra):
+        rows.add((int(rng.integers(B)), int(rng.integers(T)), int(rng.integers(Hq))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["lookup16", "batched", "maxctx"])
+def test_full_size_configs_sampled_rows(name):
+    w = config(name)
+    out, lse, info = run_gpu(w)
+    rows = _sample_rows(w, n_extra=8 if name == "maxctx" else 16)
+    ref_o, ref_l = oracle.verify_attn_rows(w, rows)
+    got_o = np.stack([out[b, t, h] for b, t, h in rows])
+    got_l = np.array([lse[b, t, h] for b, t, h in rows])
+    compare(got_o, got_l, ref_o, ref_l, f"{name} {info}")
+    # properties at full size: every output finite, every lse finite and at
+    # least the largest visible score (lse >= max_j s_j >= s of some key)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------ shape sweep
+SWEEP = []
+for T in (1, 5, 8, 16):
+    for G in (1, 4, 6, 8):
+        for i, D in enumerate((64, 128, 256)):
+            dt = ("bf16", "fp8_e4m3", "int8")[(T + G + i) % 3]
+            SWEEP.append((T, G, D, dt))
+
+
+@pytest.mark.parametrize("T,G,D,dt", SWEEP)
+def test_shape_sweep(T, G, D, dt):
+    Hkv = 2
+    lens = [T, 16 + T, 203, 77 + T]  # shortest possible, < 1 page + T, ragged tails
+    w = wl.make_workload(1000 + T * 31 + G * 7 + D, lens, T, G * Hkv, Hkv, D, dt, extra_pages=2)
+    out, lse, info = run_gpu(w, {"tokens_per_split": 64})
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"T{T} G{G} D{D} {dt} {info}")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8"])
+@pytest.mark.parametrize("split", [32, 64, 100, 512, 0])
+def test_split_count_invariance(dt, split):
+    w = wl.make_workload(77, [1234, 517], 8, 12, 2, 128, dt)
+    out, lse, info = run_gpu(w, {"tokens_per_split": split})
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"split {split} {info}")
+
+
+def test_page_permutation_bitwise_for_fixed_plan():
+    w = wl.make_workload(91, [700, 333], 5, 24, 4, 256, "int8", extra_pages=5)
+    out1, lse1, _ = run_gpu(w, {"tokens_per_split": 128})
+    perm = np.random.default_rng(4).permutation(w["num_pages"])
+    w2 = dict(w)
+    for key in ("k_pages", "v_pages", "k_scale", "v_scale"):
+        a = np.empty_like(w[key])
+        a[perm] = w[key]
+        w2[key] = a
+    w2["block_table"] = perm[w["block_table"]].astype(np.int32)
+    out2, lse2, _ = run_gpu(w2, {"tokens_per_split": 128})
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+def test_block_table_stride_and_side_stream():
+    w = wl.make_workload(93, [150, 90], 4, 8, 2, 64, "fp8_e4m3", bt_stride=40)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse, info = run_gpu(w, {"block_table_stride": 40}, stream=s)
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, "stride40")
+
+
+# ------------------------------------------------------------ checks and errors
+def test_bad_page_is_skipped_and_flagged():
+    """A block-table entry at or above the planned pool size is skipped and
+    flagged.  The entry used still lies inside the allocation (the pool is
+    allocated larger than the size given to the planner), so the access is
+    in bounds whether or not the check works."""
+    import speculative_decoding_verify_causal_gb300 as va
+    w = wl.make_workload(95, [100], 2, 4, 1, 64, "int8", extra_pages=10)
+    n_used = 7  # pages 0..6 hold the sequence after renumbering below
+    # renumber so that the sequence uses pages 0..6 and pages 7..16 are spare
+    order = w["block_table"][0, :n_used]
+    w["k_pages"][:n_used] = w["k_pages"][order]
+    w["v_pages"][:n_used] = w["v_pages"][order]
+    w["k_scale"][:n_used] = w["k_scale"][order]
+    w["v_scale"][:n_used] = w["v_scale"][order]
+    w["block_table"][0, :n_used] = np.arange(n_used)
+    d = wl.to_device(w)
+    d["block_table"][0, 3] = 12  # allocated, but >= num_pages given below
+    plan = va.verify_attn_plan(w["seq_lens"], 2, 4, 1, 64, "int8", num_pages=10)
+    try:
+        va.verify_attn_with_plan(plan, d["q"], d["k_pages"], d["v_pages"], d["k_scale"], d["v_scale"],
+                                 d["block_table"], d["seq_lens"], 2, d["out"], d["lse"])
+        flags = va.verify_attn_plan_device_flags(plan)
+        assert flags & 1
+        assert va.verify_attn_plan_device_flags(plan) == 0  # cleared
+        assert torch.isfinite(d["out"].float()).all()
+    finally:
+        plan.destroy()
+
+
+def test_seq_len_mismatch_is_flagged():
+    import speculative_decoding_verify_causal_gb300 as va
+    w = wl.make_workload(97, [100], 2, 4, 1, 64, "bf16")
+    d = wl.to_device(w)
+    d["seq_lens"][0] = 99
+    plan = va.verify_attn_plan(w["seq_lens"], 2, 4, 1, 64, "bf16")
+    try:
+        va.verify_attn_with_plan(plan, d["q"], d["k_pages"], d["v_pages"], None, None,
+                                 d["block_table"], d["seq_lens"], 2, d["out"], d["lse"])
+        assert va.verify_attn_plan_device_flags(plan) & 2
+    finally:
+        plan.destroy()
+
+
+def test_error_codes_through_the_abi():
+    import speculative_decoding_verify_causal_gb300 as va
+    lib = va.library()
+    w = wl.make_workload(99, [64], 4, 8, 2, 64, "int8")
+    d = wl.to_device(w)
+    plan = va.verify_attn_plan(w["seq_lens"], 4, 8, 2, 64, "int8")
+    P = ctypes.c_void_p
+    ptrs = [P(d[k].data_ptr()) for k in ("q", "k_pages", "v_pages", "k_scale", "v_scale", "block_table",
+                                         "seq_lens")]
+    outp, lsep = P(d["out"].data_ptr()), P(d["lse"].data_ptr())
+    try:
+        assert lib.verify_attn_with_plan(plan.handle, *ptrs, 5, outp, lsep, P(0)) == -3  # T mismatch
+        bad = list(ptrs)
+        bad[3] = P(0)  # quantised cache without k_scale
+        assert lib.verify_attn_with_plan(plan.handle, *bad, 4, outp, lsep, P(0)) == -1
+        assert lib.verify_attn_with_plan(plan.handle, *ptrs, 4, P(0), lsep, P(0)) == -1
+        # the 11-argument form uses the thread's current plan
+        assert lib.verify_attn(*ptrs, 4, outp, P(0), P(0)) == 0
+        torch.cuda.synchronize()
+        ref_out, _ = oracle.verify_attn(w)
+        compare(d["out"].float().cpu().numpy(), np.zeros_like(ref_out[..., 0]),
+                ref_out, np.zeros_like(ref_out[..., 0]), "current-plan form")
+    finally:
+        plan.destroy()
+    assert lib.verify_attn(*ptrs, 4, outp, lsep, P(0)) == -4  # destroyed -> no current plan
