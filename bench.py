@@ -263,6 +263,10 @@ def run_ours(args):
     # event pair around every partial-attention kernel
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(copies)]
+    for a, b in ev_pairs:  # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
 
     def capture(n, with_events):
         g = torch.cuda.CUDAGraph()
