@@ -88,7 +88,9 @@ typedef enum {
     VA_ERR_NO_PLAN = -4,          /* verify_attn with no current plan on this thread */
     VA_ERR_CUDA = -5,             /* a CUDA runtime call or launch failed */
     VA_ERR_OUT_OF_MEMORY = -6,    /* workspace allocation failed */
-    VA_ERR_NO_DEVICE = -7         /* no usable CUDA device */
+    VA_ERR_NO_DEVICE = -7,        /* no usable CUDA device */
+    VA_ERR_SCRATCH_TOO_SMALL = -8 /* verify_attn_noalloc: the work list alone does not
+                                     fit in VA_NOALLOC_SCRATCH_BYTES */
 } va_status;
 
 /* Which partial-attention kernel a plan uses. */
@@ -185,6 +187,44 @@ int verify_attn_plan_device_flags(const va_plan *plan, int clear, int *flags,
  * cudaEvent_t handles owned by the caller; pass NULL, NULL to stop.  Works
  * under CUDA-graph capture (the records become graph nodes). */
 int verify_attn_plan_set_events(va_plan *plan, void *ev_before, void *ev_after);
+
+/* Size of the library's built-in scratch for verify_attn_noalloc: a
+ * file-scope device array that every GPU which loads the library holds until
+ * the process exits. */
+#define VA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Verify attention without any memory allocation, for callers that cannot
+ * call cudaMalloc: code running where the allocator is off limits (inside a
+ * custom memory pool's accounting, a real-time or signal-safe path, or an
+ * embedding runtime that owns all device memory), or that must not grow the
+ * device footprint after start-up.  (The paper has no counterpart: this entry
+ * exists for deployment.)
+ *
+ * It plans from seq_lens_host on every call (host work only, no heap) and
+ * keeps the work list and the split partials in a static device array of
+ * VA_NOALLOC_SCRATCH_BYTES instead of a plan's workspace.  The caller passes
+ * every input and output exactly as for verify_attn (same layouts), plus the
+ * block-table row stride (0 = max_b ceil(L_b / 16)).  When the partials of
+ * the default split do not fit, the split is made coarser until they do; a
+ * problem whose work list alone does not fit returns
+ * VA_ERR_SCRATCH_TOO_SMALL.  Nothing is allocated: no cudaMalloc, no
+ * cudaFree, no allocating library call.
+ *
+ * The first call on a device looks up the array's device address there
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array, and each call
+ * overwrites what the previous one left there (its flag word is cleared at
+ * the start of every call): calls that overlap on the GPU race, so order them
+ * on one stream.  Asynchronous like verify_attn; the host-to-device copy of
+ * the work list is made from pageable host memory. */
+int verify_attn_noalloc(const int32_t *seq_lens_host, int num_seqs, int T,
+                        int num_q_heads, int num_kv_heads, int head_dim,
+                        va_kv_dtype kv_dtype, const void *q,
+                        const void *k_pages, const void *v_pages,
+                        const float *k_scale, const float *v_scale,
+                        const int32_t *block_table, int block_table_stride,
+                        const int32_t *seq_lens, void *out, float *lse,
+                        void *stream);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ PAGE_SIZE = 16
 STATUS_NAMES = {
     0: "VA_OK", -1: "VA_ERR_INVALID_ARGUMENT", -2: "VA_ERR_UNSUPPORTED",
     -3: "VA_ERR_PLAN_MISMATCH", -4: "VA_ERR_NO_PLAN", -5: "VA_ERR_CUDA",
-    -6: "VA_ERR_OUT_OF_MEMORY", -7: "VA_ERR_NO_DEVICE",
+    -6: "VA_ERR_OUT_OF_MEMORY", -7: "VA_ERR_NO_DEVICE", -8: "VA_ERR_SCRATCH_TOO_SMALL",
 }
 
 
@@ -87,6 +87,8 @@ def _load():
         lib.verify_attn_plan_device_flags.argtypes = [P, I, ctypes.POINTER(I), P]
         lib.verify_attn_plan_set_events.argtypes = [P, P, P]
         lib.verify_attn_plan_set_events.restype = I
+        lib.verify_attn_noalloc.argtypes = [P, I, I, I, I, I, I] + [P] * 6 + [I, P, P, P, P]
+        lib.verify_attn_noalloc.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
                   "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
             getattr(lib, f).restype = I
@@ -293,7 +295,26 @@ def verify_attn_plan_set_events(plan: Plan, ev_before=None, ev_after=None):
     _check(_load().verify_attn_plan_set_events(plan.handle, b, a), "verify_attn_plan_set_events")
 
 
+def verify_attn_noalloc(seq_lens_host, T, num_q_heads, num_kv_heads, head_dim, kv_dtype, q, k_pages,
+                        v_pages, k_scale, v_scale, block_table, seq_lens, out, lse=None,
+                        block_table_stride=0, stream=None):
+    """Verify attention that allocates no device memory: plans from the host
+    ``seq_lens_host`` on every call and keeps its scratch in the library's
+    static device array (see ``include/verify_attn.h``).  For callers that
+    cannot call cudaMalloc.  Calls share that array, so order them on one
+    stream; make the first call on a device before any stream capture."""
+    lens = _host_lens(seq_lens_host)
+    code = _dtype_code(kv_dtype)
+    args, tail, s = _marshal(code, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
+                             stream)
+    rc = _load().verify_attn_noalloc(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T), int(num_q_heads),
+                                     int(num_kv_heads), int(head_dim), code, *args[:6],
+                                     int(block_table_stride), args[6], *tail, s)
+    _check(rc, "verify_attn_noalloc")
+
+
 __all__ = [
+    "verify_attn_noalloc",
     "verify_attn_plan_set_events",
     "verify_attn_plan", "verify_attn", "verify_attn_with_plan", "verify_attn_plan_destroy",
     "verify_attn_status_string", "verify_attn_plan_get_info", "verify_attn_plan_describe",

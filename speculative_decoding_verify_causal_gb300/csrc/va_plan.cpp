@@ -269,6 +269,8 @@ const char *verify_attn_status_string(int status) {
     case VA_ERR_CUDA: return "CUDA runtime error";
     case VA_ERR_OUT_OF_MEMORY: return "device workspace allocation failed";
     case VA_ERR_NO_DEVICE: return "no usable CUDA device";
+    case VA_ERR_SCRATCH_TOO_SMALL:
+        return "work list exceeds the static scratch of verify_attn_noalloc (VA_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
     }
 }

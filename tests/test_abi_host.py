@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         s = va.verify_attn_status_string(code)
         assert s and s != "unknown status"
     assert va.verify_attn_status_string(-99) == "unknown status"
