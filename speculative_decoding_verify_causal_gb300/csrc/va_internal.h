@@ -57,11 +57,16 @@ cudaError_t launch_warp_partial(const PartialParams &p, int head_dim, int kv_dty
                                 int num_items, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, int num_groups, int max_splits,
                            cudaStream_t s);
+cudaError_t launch_mma_partial(const PartialParams &p, int head_dim, int kv_dtype,
+                               int num_items, cudaStream_t s);
+size_t mma_smem_bytes(int head_dim, int kv_dtype, int num_kv_heads);
 
 // Geometry of each path.
 constexpr int kWarpRows = 16;    // packed rows per work item, CUDA-core kernel
 constexpr int kWarpTile = 32;    // keys per smem tile, CUDA-core kernel
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
 constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
+constexpr int kMmaMinRows = 16;  // packed rows from which the planner picks tcgen05
+constexpr int kMmaMaxKvHeads = 16;  // scale blocks of larger pools do not fit its smem
 
 }  // namespace va

@@ -101,22 +101,24 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
     return VA_OK;
 }
 
-int choose_path(int R, const va_plan_options *opts) {
+// Tensor cores once the packed rows of a kv head (G * T) reach an MMA row
+// tile's worth of work; CUDA-core dot products below that.
+int choose_path(int R, int Hkv, const va_plan_options *opts) {
     int want = opts ? opts->path : VA_PATH_AUTO;
     if (want != VA_PATH_AUTO) return want;
-    (void)R;
-    return VA_PATH_WARP;
+    return (R >= va::kMmaMinRows && Hkv <= va::kMmaMaxKvHeads) ? VA_PATH_MMA : VA_PATH_WARP;
 }
 
 int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int dtype,
                   int num_sms, const va_plan_options *opts, Geometry &g) {
     const int G = Hq / Hkv;
     const int R = G * T;
-    g.path = choose_path(R, opts);
-    if (g.path == VA_PATH_MMA) return VA_ERR_UNSUPPORTED;  // not in this build yet
-    const int max_rows = va::kWarpRows;
-    g.tile = va::kWarpTile;
-    g.slots = num_sms * 2;
+    g.path = choose_path(R, Hkv, opts);
+    if (g.path == VA_PATH_MMA && Hkv > va::kMmaMaxKvHeads) return VA_ERR_UNSUPPORTED;
+    const bool mma = g.path == VA_PATH_MMA;
+    const int max_rows = mma ? va::kMmaRows : va::kWarpRows;
+    g.tile = mma ? va::kMmaTile : va::kWarpTile;
+    g.slots = mma ? num_sms : num_sms * 2;  // the tcgen05 kernel holds a whole SM (TMEM, smem)
     g.num_row_groups = (R + max_rows - 1) / max_rows;
     g.rows_per_group = (R + g.num_row_groups - 1) / g.num_row_groups;
 
@@ -131,7 +133,7 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
     // pipeline fill) and, for split sequences, the partial write + combine
     // read of rows x D fp32 relative to one token's KV bytes.
     const double token_bytes = 2.0 * D * kv_bytes(dtype) + (dtype == VA_BF16 ? 0 : 8);
-    const double c_item = 128.0;
+    const double c_item = mma ? 384.0 : 128.0;
     const double c_split = 2.0 * g.rows_per_group * (D + 1) * 4.0 / token_bytes;
 
     auto cost_of = [&](int c, std::vector<double> *costs) {
@@ -161,7 +163,7 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
         std::vector<int> cand;
         const double units = total * per_seq_items;
         for (double waves : {0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 8.0}) {
-            double c = units / (g.slots * waves) / per_seq_items;
+            double c = units / (g.slots * waves);  // key tokens per item for `waves` items per slot
             int ci = (int)std::ceil(c / g.tile) * g.tile;
             ci = std::max(ci, 4 * g.tile);
             cand.push_back(ci);
@@ -465,10 +467,22 @@ int verify_attn_with_plan(const va_plan *p, const void *q, const void *k_pages,
     pp.num_pages = p->num_pages;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->D));
 
+    if (p->path == VA_PATH_MMA) {
+        // TMA and bulk copies need 16-byte aligned bases
+        auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+        if (misaligned(k_pages) || misaligned(v_pages) || misaligned(q) || misaligned(out) ||
+            (p->kv_dtype != VA_BF16 && (misaligned(k_scale) || misaligned(v_scale))))
+            return VA_ERR_INVALID_ARGUMENT;
+    }
     if (p->ev_before && cudaEventRecordWithFlags(p->ev_before, s, cudaEventRecordExternal) != cudaSuccess)
         return VA_ERR_CUDA;
-    cudaError_t e = va::launch_warp_partial(pp, p->D, p->kv_dtype, p->num_items, s);
-    if (e != cudaSuccess) return VA_ERR_CUDA;
+    cudaError_t e = p->path == VA_PATH_MMA
+                        ? va::launch_mma_partial(pp, p->D, p->kv_dtype, p->num_items, s)
+                        : va::launch_warp_partial(pp, p->D, p->kv_dtype, p->num_items, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return VA_ERR_CUDA;
+    }
     if (p->ev_after && cudaEventRecordWithFlags(p->ev_after, s, cudaEventRecordExternal) != cudaSuccess)
         return VA_ERR_CUDA;
     if (p->num_groups > 0) {

@@ -79,7 +79,7 @@ def _check_cover(lens, T, Hq, Hkv, items, info):
     (list(np.random.default_rng(3).integers(1000, 8001, 64) + 5), 5, 24, 4, 256, "fp8_e4m3"),
     ([1, 2, 3, 17, 33], 1, 8, 8, 128, "bf16"),
 ])
-@pytest.mark.parametrize("path", ["warp"])
+@pytest.mark.parametrize("path", ["warp", "mma", "auto"])
 def test_planner_covers_every_key_once(lens, T, Hq, Hkv, D, dt, path):
     lens = [int(x) for x in lens]
     T = min(T, min(lens))
@@ -93,6 +93,16 @@ def test_planner_fills_the_chip_for_one_long_sequence():
     info, items = va.verify_attn_plan_describe([25016], 16, 24, 4, 256, "int8", num_sms=148, path="warp")
     assert info["num_items"] >= 148
     assert info["max_splits"] > 1
+
+
+def test_planner_picks_tensor_cores_from_an_mma_tile_of_rows():
+    # G*T >= 16 packed rows -> tcgen05 kernel; fewer -> CUDA-core kernel
+    big, _ = va.verify_attn_plan_describe([25016], 16, 24, 4, 256, "int8", num_sms=148)
+    small, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148)
+    assert big["path"] == 2 and small["path"] == 1
+    assert big["rows_per_group"] == 96 and big["num_row_groups"] == 1
+    # one CTA per SM for the tensor-core kernel: about one wave of items
+    assert 148 * 0.75 <= big["num_items"] <= 148
 
 
 def test_planner_uses_live_lengths_only():
