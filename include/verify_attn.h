@@ -188,6 +188,12 @@ int verify_attn_plan_device_flags(const va_plan *plan, int clear, int *flags,
  * under CUDA-graph capture (the records become graph nodes). */
 int verify_attn_plan_set_events(va_plan *plan, void *ev_before, void *ev_after);
 
+/* The cudaError_t value of the most recent CUDA call made by this library on
+ * the calling thread that failed (0 if none): the detail behind a
+ * VA_ERR_CUDA status.  verify_attn_last_cuda_error_string gives its text. */
+int verify_attn_last_cuda_error(void);
+const char *verify_attn_last_cuda_error_string(void);
+
 /* Size of the library's built-in scratch for verify_attn_noalloc: a
  * file-scope device array that every GPU which loads the library holds until
  * the process exits. */

@@ -40,7 +40,12 @@ STATUS_NAMES = {
 class VerifyAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({verify_attn_status_string(status)})")
+        msg = f"{what}: {STATUS_NAMES.get(status, status)} ({verify_attn_status_string(status)})"
+        if status == -5:
+            lib = _load()
+            msg += f" [cuda error {lib.verify_attn_last_cuda_error()}: " \
+                   f"{lib.verify_attn_last_cuda_error_string().decode()}]"
+        super().__init__(msg)
 
 
 class _Options(ctypes.Structure):
@@ -87,6 +92,10 @@ def _load():
         lib.verify_attn_plan_device_flags.argtypes = [P, I, ctypes.POINTER(I), P]
         lib.verify_attn_plan_set_events.argtypes = [P, P, P]
         lib.verify_attn_plan_set_events.restype = I
+        lib.verify_attn_last_cuda_error.argtypes = []
+        lib.verify_attn_last_cuda_error.restype = I
+        lib.verify_attn_last_cuda_error_string.argtypes = []
+        lib.verify_attn_last_cuda_error_string.restype = ctypes.c_char_p
         lib.verify_attn_noalloc.argtypes = [P, I, I, I, I, I, I] + [P] * 6 + [I, P, P, P, P]
         lib.verify_attn_noalloc.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",

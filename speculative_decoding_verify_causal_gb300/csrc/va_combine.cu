@@ -60,15 +60,31 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 
     const int t = rr / p.G, h = g.kvh * p.G + rr % p.G;
     const size_t orow = (size_t)(g.b * p.T + t) * p.Hq + h;
-    for (int d = tid; d < p.D; d += kThreads) {
-        float acc = 0.f;
-        for (int s = 0; s < n; ++s) {
-            const float ws = w[s];
-            if (ws != 0.f)
-                acc = fmaf(ws, p.o_part[((size_t)(g.first_part + s) * p.rows_per_group + r) * p.D + d], acc);
+    __syncthreads();  // w[] complete
+    // Thread owns two adjacent columns; eight splits are loaded before any is
+    // accumulated so that the loads overlap.
+    const size_t pstride = (size_t)p.rows_per_group * p.D;  // floats between splits
+    const float *base = p.o_part + ((size_t)g.first_part * p.rows_per_group + r) * p.D;
+    for (int d = 2 * tid; d < p.D; d += 2 * kThreads) {
+        float2 acc = make_float2(0.f, 0.f);
+        int s = 0;
+        for (; s + 8 <= n; s += 8) {
+            float2 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const float2 *>(base + (s + k) * pstride + d);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc.x = fmaf(w[s + k], v[k].x, acc.x);
+                acc.y = fmaf(w[s + k], v[k].y, acc.y);
+            }
         }
-        __nv_bfloat16 o = __float2bfloat16_rn(acc * inv);
-        p.out[orow * p.D + d] = *reinterpret_cast<uint16_t *>(&o);
+        for (; s < n; ++s) {
+            const float2 v = *reinterpret_cast<const float2 *>(base + s * pstride + d);
+            acc.x = fmaf(w[s], v.x, acc.x);
+            acc.y = fmaf(w[s], v.y, acc.y);
+        }
+        __nv_bfloat162 o = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(p.out + orow * p.D + d) = o;
     }
     if (tid == 0 && p.lse) p.lse[orow] = z > 0.f ? m + logf(z) : -INFINITY;
 }

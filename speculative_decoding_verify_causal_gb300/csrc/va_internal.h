@@ -52,6 +52,9 @@ struct CombineParams {
     int T, Hq, G, R, rows_per_group, D;
 };
 
+// Remember a failing CUDA call for verify_attn_last_cuda_error (thread-local).
+void note_cuda_error(cudaError_t e);
+
 // Kernel launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_warp_partial(const PartialParams &p, int head_dim, int kv_dtype,
                                 int num_items, cudaStream_t s);
@@ -67,6 +70,7 @@ constexpr int kWarpTile = 32;    // keys per smem tile, CUDA-core kernel
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
 constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
 constexpr int kMmaMinRows = 16;  // packed rows from which the planner picks tcgen05
-constexpr int kMmaMaxKvHeads = 16;  // scale blocks of larger pools do not fit its smem
+constexpr int kMmaMaxItemTokens = 16384;  // longest split of the tcgen05 kernel (page ids in smem)
+constexpr size_t kMaxSmemPerBlock = 232448;  // opt-in dynamic shared memory per block (227 KB)
 
 }  // namespace va

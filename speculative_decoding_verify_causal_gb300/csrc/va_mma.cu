@@ -51,12 +51,13 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = kMmaTile;     // keys per S tile (MMA N)
-constexpr int kRawKeys = 32;        // keys per raw (8-bit) stage: 2 pages
-constexpr int kRawStages = 4;
+constexpr int kMaxRawStages = 6;    // raw (8-bit) stages: one 64-key K or V tile each
+constexpr int kMinRawStages = 3;
 constexpr int kBfStages = 3;        // bf16: 64-key stages TMA'd straight into MMA layout
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kScaleRing = 4;       // per-tile k/v scales handed to the softmax warps
+constexpr int kMaxItemPages = kMmaMaxItemTokens / VA_PAGE_SIZE;  // page ids staged in smem
 
 enum : int { kFlagTimeout = 4 };
 
@@ -64,6 +65,7 @@ struct MmaParams {
     CUtensorMap tm_k;  // 64-byte aligned members first
     CUtensorMap tm_v;
     PartialParams p;
+    int raw_stages;    // quantised caches: stages of the raw ring (fits the smem budget)
 };
 
 template <int D, int DT>
@@ -72,8 +74,14 @@ struct Cfg {
     static constexpr int kNumBuf = kQuant ? 2 : kBfStages;
     static constexpr int kConvBytes = kTile * D * 2;   // K or V tile, 16-bit, SW128 chunks of 64 d
     static constexpr int kChunkBytes = kTile * 128;    // one 64-d chunk of a tile
-    static constexpr int kRawBytes = kRawKeys * D;     // K or V half tile, 8-bit
-    static constexpr int kWarps = kQuant ? 10 : 6;
+    static constexpr int kRawTileBytes = kTile * D;    // one K or V tile, 8-bit
+    // warps 0-7 softmax (two per TMEM lane quarter), 8-11 dequant (quantised
+    // caches only), then the producer and the MMA issuer
+    static constexpr int kSoftmaxWarps = 8;
+    static constexpr int kDequantWarps = kQuant ? 8 : 0;
+    static constexpr int kProducerWarp = kSoftmaxWarps + kDequantWarps;
+    static constexpr int kMmaWarp = kProducerWarp + 1;
+    static constexpr int kWarps = kMmaWarp + 1;
     static constexpr int kThreads = kWarps * 32;
     static constexpr uint32_t kQCol = 0;
     static constexpr uint32_t kOCol = D / 2;
@@ -81,36 +89,38 @@ struct Cfg {
     static constexpr uint32_t kTmemCols = 512;
 };
 
-// Shared memory carve-up (byte offsets from a 1024-aligned base).
+// Shared memory carve-up (byte offsets from a 1024-aligned base).  The raw
+// ring (quantised caches) holds one pass per stage, in the order the dequant
+// warps consume them: K of tile 0, V of tile 0, K of tile 1, ...
 template <int D, int DT>
 struct Smem {
     using C = Cfg<D, DT>;
-    uint32_t conv_k, conv_v;       // kNumBuf buffers each
-    uint32_t raw, raw_stride;      // kRawStages stages (quantised only)
-    uint32_t raw_v, raw_ks, raw_vs;  // offsets inside a raw stage
-    uint32_t scale_ring;           // kScaleRing x (64 k + 64 v) floats
-    uint32_t bars;                 // mbarriers
+    uint32_t conv_k, conv_v;         // kNumBuf buffers each
+    uint32_t raw, raw_stride;        // raw stages
+    uint32_t pids;                   // the item's page ids (kMaxItemPages ints)
+    uint32_t scale_ring;             // kScaleRing x (64 k + 64 v) floats
+    uint32_t xchg;                   // softmax pair exchange: [2][2][128] maxima + [2][128] sums
+    uint32_t bars;                   // mbarriers
     uint32_t total;
-    __host__ __device__ explicit Smem(int Hkv) {
+    __host__ __device__ Smem(int Hkv, int nst) {
         conv_k = 0;
         conv_v = conv_k + C::kNumBuf * C::kConvBytes;
         raw = conv_v + C::kNumBuf * C::kConvBytes;
-        const uint32_t sc = 2u * VA_PAGE_SIZE * Hkv * 4;  // one stage's scale blocks (2 pages)
-        raw_v = C::kRawBytes;
-        raw_ks = 2 * C::kRawBytes;
-        raw_vs = raw_ks + sc;
-        raw_stride = C::kQuant ? ((raw_vs + sc + 127) / 128 * 128) : 0;
-        scale_ring = raw + (C::kQuant ? kRawStages * raw_stride : 0);
-        bars = scale_ring + (C::kQuant ? kScaleRing * 2 * kTile * 4 : 0);
+        (void)Hkv;
+        raw_stride = C::kQuant ? C::kRawTileBytes : 0;
+        pids = raw + (C::kQuant ? nst * raw_stride : 0);
+        scale_ring = pids + kMaxItemPages * 4;
+        xchg = scale_ring + (C::kQuant ? kScaleRing * 2 * kTile * 4 : 0);
+        bars = xchg + 6 * 128 * 4;
         total = bars + 64 * 8 + 16;
     }
 };
 
 // Barrier slots (8 bytes each) inside Smem::bars.
 enum Bar : int {
-    kRawFull = 0,                       // kRawStages
-    kRawEmpty = kRawFull + kRawStages,  // kRawStages
-    kKFull = kRawEmpty + kRawStages,    // kNumBuf (<= 3)
+    kRawFull = 0,                          // kMaxRawStages
+    kRawEmpty = kRawFull + kMaxRawStages,  // kMaxRawStages
+    kKFull = kRawEmpty + kMaxRawStages,    // kNumBuf (<= 3)
     kKEmpty = kKFull + 3,
     kVFull = kKEmpty + 3,
     kVEmpty = kVFull + 3,
@@ -124,6 +134,13 @@ enum Bar : int {
 };
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// 2^x with the hardware approximation (relative error ~2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -170,7 +187,8 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const Smem<D, DT> L(p.Hkv);
+    const int nst = C::kQuant ? mp.raw_stages : 1;  // raw stages (quantised caches only)
+    const Smem<D, DT> L(p.Hkv, nst);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + L.bars;
     auto bar = [&](int i) { return bar0 + 8u * i; };
@@ -186,103 +204,206 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     const int32_t *bt = p.block_table + (size_t)it.b * p.bt_stride;
 
     if (tid == 0) {
-        for (int i = 0; i < kRawStages; ++i) {
+        for (int i = 0; i < kMaxRawStages; ++i) {
             mbar_init(bar(kRawFull + i), 1);
-            mbar_init(bar(kRawEmpty + i), 4);
+            mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps : 1);
         }
         for (int i = 0; i < 3; ++i) {
-            mbar_init(bar(kKFull + i), C::kQuant ? 4 : 1);
-            mbar_init(bar(kVFull + i), C::kQuant ? 4 : 1);
+            mbar_init(bar(kKFull + i), C::kQuant ? C::kDequantWarps : 1);
+            mbar_init(bar(kVFull + i), C::kQuant ? C::kDequantWarps : 1);
             mbar_init(bar(kKEmpty + i), 1);
             mbar_init(bar(kVEmpty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kSFull + i), 1);
             mbar_init(bar(kSFree + i), 1);
-            mbar_init(bar(kPFull + i), 4);
+            mbar_init(bar(kPFull + i), C::kSoftmaxWarps);
         }
         mbar_init(bar(kODone), 1);
         mbar_init(bar(kOFinal), 1);
-        mbar_init(bar(kQReady), 4);
+        mbar_init(bar(kQReady), C::kSoftmaxWarps + C::kDequantWarps);
         fence_barrier_init();
         if (p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);
     }
-    if (warp == 1) {
+    if (warp == C::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
+    }
+    // Q rows are written to TMEM by the warps of each lane quarter: the two
+    // softmax warps and (quantised caches) the two dequant warps of quarter
+    // q = warp % 4 each take one part of the row's d range.  The loads are
+    // issued now, one round trip overlapping the set-up.
+    constexpr int kQParts = C::kQuant ? 4 : 2;
+    constexpr int kQv = D / 8 / kQParts;  // 16-byte loads per part
+    const bool q_warp = warp < C::kSoftmaxWarps + C::kDequantWarps;
+    const int q_part = warp < C::kSoftmaxWarps ? (warp >> 2) : 2 + ((warp - C::kSoftmaxWarps) >> 2);
+    uint4 qv[kQv];
+    int t_r = 0;
+    if (q_warp) {
+        const int r = (warp & 3) * 32 + lane;
+        if (r < nrows) {
+            const int rr = row0 + r;
+            t_r = rr / G;
+            const int h = it.kvh * G + rr % G;
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)(it.b * T + t_r) * p.Hq + h) * D) +
+                                q_part * kQv;
+#pragma unroll
+            for (int k = 0; k < kQv; ++k) qv[k] = __ldg(qrow + k);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kQv; ++k) qv[k] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    const int lp0 = it.k_begin / VA_PAGE_SIZE;                               // first logical page
+    const int npages_item = (it.k_end + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE - lp0;
+    if (warp == C::kProducerWarp) {
+        // the item's page ids -> smem (bad entries replaced by page 0 and flagged)
+        for (int k = lane; k < npages_item; k += 32) {
+            int page = bt[lp0 + k];
+            if (p.num_pages > 0 && (page < 0 || page >= p.num_pages)) {
+                atomicOr(p.flags, kFlagBadPage);
+                page = 0;
+            }
+            sts_u32(sbase + L.pids + 4u * k, (uint32_t)page);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    float q_prescale = 1.f;  // power of two folded into fp16 q (quantised caches)
+    if (q_warp) {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_tm = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t xq = sbase + L.xchg;  // [part][128] row maxima
+        if (C::kQuant) {
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < kQv; ++k) {
+                const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[e] & 0xFFFFu)),
+                                             fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+            }
+            sts_f32(xq + 4u * (q_part * 128 + r), amax);
+            named_bar_sync(5 + quarter, 32 * kQParts);
+#pragma unroll
+            for (int o = 0; o < kQParts; ++o) amax = fmaxf(amax, lds_f32(xq + 4u * (o * 128 + r)));
+            named_bar_sync(5 + quarter, 32 * kQParts);  // the slots are reused by the softmax
+            if (amax > 0.f) {
+                int e;
+                frexpf(amax, &e);                     // amax in [2^(e-1), 2^e)
+                q_prescale = exp2f((float)(15 - e));  // amax * prescale in [2^14, 2^15): exact fp16
+            }
+        }
+        // two bf16 -> one TMEM column; this part is columns [q_part * 4 kQv, +4 kQv)
+        constexpr int kCols = 4 * kQv < 32 ? 4 * kQv : 32;
+        const uint32_t qcol = lane_tm + C::kQCol + q_part * 4 * kQv;
+#pragma unroll
+        for (int c0 = 0; c0 < 4 * kQv; c0 += kCols) {
+            uint32_t v[kCols];
+#pragma unroll
+            for (int k = 0; k < kCols / 4; ++k) {
+                const uint4 x = qv[c0 / 4 + k];
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (C::kQuant)
+                        v[4 * k + e] = pack_half2(bf16_bits_to_float(w[e] & 0xFFFFu) * q_prescale,
+                                                  __uint_as_float(w[e] & 0xFFFF0000u) * q_prescale);
+                    else
+                        v[4 * k + e] = w[e];
+                }
+            }
+            if constexpr (kCols == 8)
+                tmem_st8(qcol + c0, *reinterpret_cast<uint32_t(*)[8]>(&v[0]));
+            else if constexpr (kCols == 16)
+                tmem_st16(qcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            else
+                tmem_st32(qcol + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kQReady));
+    }
 
-    if (warp == 0) {
+    if (warp == C::kProducerWarp) {
         // ------------------------------------------------------------ producer
+        // The whole warp walks the stages; lane pg issues the TMA box of the
+        // tile's page pg (page ids come from smem, staged at kernel start).
         if (lane == 0) {
             prefetch_tensormap(&mp.tm_k);
             prefetch_tensormap(&mp.tm_v);
-            if (C::kQuant) {
-                const int nraw = (nkeys + kRawKeys - 1) / kRawKeys;
-                const uint32_t page_bytes = VA_PAGE_SIZE * D;          // one page, one head, 8-bit
-                const uint32_t scale_bytes = VA_PAGE_SIZE * Hkv * 4;   // one page's scale block
-                int issued = 0;
-                for (int rs = 0; rs < nraw && ok; ++rs) {
-                    const int slot = rs % kRawStages, use = rs / kRawStages;
-                    if (!mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs)) { ok = false; break; }
-                    const int key0 = it.k_begin + rs * kRawKeys;
-                    const int npg = min(2, (it.k_end - key0 + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE);
-                    const uint32_t st = sbase + L.raw + slot * L.raw_stride;
-                    mbar_arrive_expect_tx(bar(kRawFull + slot), npg * 2 * (page_bytes + scale_bytes));
-                    for (int pg = 0; pg < npg; ++pg) {
-                        int page = bt[key0 / VA_PAGE_SIZE + pg];
-                        if (p.num_pages > 0 && (page < 0 || page >= p.num_pages)) {
-                            atomicOr(p.flags, kFlagBadPage);
-                            page = 0;  // load a real page; the dequant masks these keys out
-                        }
-                        tma_load_4d(st + pg * page_bytes, &mp.tm_k, 0, it.kvh, 0, page, bar(kRawFull + slot));
-                        tma_load_4d(st + L.raw_v + pg * page_bytes, &mp.tm_v, 0, it.kvh, 0, page,
-                                    bar(kRawFull + slot));
-                        bulk_load(st + L.raw_ks + pg * scale_bytes, p.k_scale + (size_t)page * VA_PAGE_SIZE * Hkv,
-                                  scale_bytes, bar(kRawFull + slot));
-                        bulk_load(st + L.raw_vs + pg * scale_bytes, p.v_scale + (size_t)page * VA_PAGE_SIZE * Hkv,
-                                  scale_bytes, bar(kRawFull + slot));
-                    }
-                    issued = rs + 1;
-                }
-                // drain: every issued copy must land before the CTA may exit
-                const int first = issued > kRawStages ? issued - kRawStages : 0;
-                for (int rs = first; rs < issued; ++rs)
-                    if (!mbar_wait(bar(kRawFull + rs % kRawStages), (rs / kRawStages) & 1, kWaitNs)) ok = false;
-            } else {
-                const uint32_t box_bytes = VA_PAGE_SIZE * 128;  // 16 rows x 64 bf16
-                int issued = 0;
-                for (int i = 0; i < ntiles && ok; ++i) {
-                    const int buf = i % C::kNumBuf, use = i / C::kNumBuf;
-                    if (!mbar_wait(bar(kKEmpty + buf), (use & 1) ^ 1, kWaitNs) ||
-                        !mbar_wait(bar(kVEmpty + buf), (use & 1) ^ 1, kWaitNs)) { ok = false; break; }
-                    const int key0 = it.k_begin + i * kTile;
-                    const int npg = min(kTile / VA_PAGE_SIZE, (it.k_end - key0 + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE);
-                    const uint32_t kb = sbase + L.conv_k + buf * C::kConvBytes;
-                    const uint32_t vb = sbase + L.conv_v + buf * C::kConvBytes;
+        }
+        auto tile_page = [&](int i) -> int {  // lane pg: page pg of tile i (0 past the end)
+            const int k = i * (kTile / VA_PAGE_SIZE) + lane;
+            return (lane < kTile / VA_PAGE_SIZE && k < npages_item) ? (int)lds_u32(sbase + L.pids + 4u * k) : 0;
+        };
+        auto tile_npg = [&](int i) {
+            return min(kTile / VA_PAGE_SIZE, npages_item - i * (kTile / VA_PAGE_SIZE));
+        };
+        if constexpr (C::kQuant) {
+            const int npass = 2 * ntiles;                          // K and V of every tile
+            const uint32_t page_bytes = VA_PAGE_SIZE * D;          // one page, one head, 8-bit
+            int issued = 0;
+            for (int ps = 0; ps < npass; ++ps) {
+                const int slot = ps % nst, use = ps / nst;
+                ok = __shfl_sync(0xffffffffu, (int)mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs), 0);
+                if (!ok) break;
+                const int i = ps >> 1, kv = ps & 1;
+                const int npg = tile_npg(i);
+                const int page = tile_page(i);
+                const uint32_t st = sbase + L.raw + slot * L.raw_stride;
+                if (lane == 0) mbar_arrive_expect_tx(bar(kRawFull + slot), npg * page_bytes);
+                __syncwarp();
+                if (lane < npg)
+                    tma_load_4d(st + lane * page_bytes, kv == 0 ? &mp.tm_k : &mp.tm_v, 0, it.kvh, 0, page,
+                                bar(kRawFull + slot));
+                __syncwarp();
+                issued = ps + 1;
+            }
+            // drain: every issued copy must land before the CTA may exit
+            if (lane == 0) {
+                const int first = issued > nst ? issued - nst : 0;
+                for (int ps = first; ps < issued; ++ps)
+                    if (!mbar_wait(bar(kRawFull + ps % nst), (ps / nst) & 1, kWaitNs)) ok = false;
+            }
+        } else {
+            const uint32_t box_bytes = VA_PAGE_SIZE * 128;  // 16 rows x 64 bf16
+            int issued = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int buf = i % C::kNumBuf, use = i / C::kNumBuf;
+                ok = __shfl_sync(0xffffffffu,
+                                 (int)(mbar_wait(bar(kKEmpty + buf), (use & 1) ^ 1, kWaitNs) &&
+                                       mbar_wait(bar(kVEmpty + buf), (use & 1) ^ 1, kWaitNs)),
+                                 0);
+                if (!ok) break;
+                const int npg = tile_npg(i);
+                const int page = tile_page(i);
+                const uint32_t kb = sbase + L.conv_k + buf * C::kConvBytes;
+                const uint32_t vb = sbase + L.conv_v + buf * C::kConvBytes;
+                if (lane == 0) {
                     mbar_arrive_expect_tx(bar(kKFull + buf), npg * (D / 64) * box_bytes);
                     mbar_arrive_expect_tx(bar(kVFull + buf), npg * (D / 64) * box_bytes);
-                    for (int pg = 0; pg < npg; ++pg) {
-                        int page = bt[key0 / VA_PAGE_SIZE + pg];
-                        if (p.num_pages > 0 && (page < 0 || page >= p.num_pages)) {
-                            atomicOr(p.flags, kFlagBadPage);
-                            page = 0;
-                        }
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c) {
-                            tma_load_4d(kb + c * C::kChunkBytes + pg * box_bytes, &mp.tm_k, c * 64, it.kvh, 0, page,
-                                        bar(kKFull + buf));
-                            tma_load_4d(vb + c * C::kChunkBytes + pg * box_bytes, &mp.tm_v, c * 64, it.kvh, 0, page,
-                                        bar(kVFull + buf));
-                        }
-                    }
-                    issued = i + 1;
                 }
+                __syncwarp();
+                if (lane < npg) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(kb + c * C::kChunkBytes + lane * box_bytes, &mp.tm_k, c * 64, it.kvh, 0, page,
+                                    bar(kKFull + buf));
+                        tma_load_4d(vb + c * C::kChunkBytes + lane * box_bytes, &mp.tm_v, c * 64, it.kvh, 0, page,
+                                    bar(kVFull + buf));
+                    }
+                }
+                __syncwarp();
+                issued = i + 1;
+            }
+            if (lane == 0) {
                 const int first = issued > C::kNumBuf ? issued - C::kNumBuf : 0;
                 for (int i = first; i < issued; ++i) {
                     if (!mbar_wait(bar(kKFull + i % C::kNumBuf), (i / C::kNumBuf) & 1, kWaitNs)) ok = false;
@@ -290,7 +411,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             constexpr int kAB = C::kQuant ? 0 : 1;  // fp16 (quantised caches) or bf16
@@ -336,92 +457,41 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             mma_commit(bar(kOFinal));
             if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         }
-    } else if (warp < 6) {
+    } else if (warp < C::kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
+        // Warps w and w+4 share TMEM lane quarter w % 4 (rows 32q..32q+31):
+        // half h = w / 4 owns S columns [32h, 32h + 32) of every tile, O
+        // columns [h D/2, (h+1) D/2) and the row's d range [h D/2, (h+1) D/2)
+        // of Q.  The pair exchanges per-row maxima through shared memory.
+        const int quarter = warp & 3, half = warp >> 2;
         const int r = quarter * 32 + lane;
         const bool row_ok = r < nrows;
-        const bool warp_active = quarter * 32 < nrows;
+        const bool warp_active = quarter * 32 < nrows;  // same for both warps of a pair
         const uint32_t lane_tm = tmem + ((uint32_t)(quarter * 32) << 16);
-        int t_r = 0;
-        float c_r = p.sm_scale_log2;  // score scale in log2 units (divided by q's power-of-two prescale)
-        // Q row -> TMEM (fp16 with an exact power-of-two prescale for
-        // quantised caches; bf16 as is)
-        {
-            const uint4 *qrow = nullptr;
-            if (row_ok) {
-                const int rr = row0 + r;
-                t_r = rr / G;
-                const int h = it.kvh * G + rr % G;
-                qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)(it.b * T + t_r) * p.Hq + h) * D);
-            }
-            float qscale = 1.f;
-            if (C::kQuant && row_ok) {
-                float amax = 0.f;
-                for (int i = 0; i < D / 8; ++i) {
-                    const uint4 v = qrow[i];
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xFFFFu)),
-                                                 fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
-                }
-                if (amax > 0.f) {
-                    int e;
-                    frexpf(amax, &e);  // amax in [2^(e-1), 2^e)
-                    qscale = exp2f((float)(15 - e));  // amax * qscale in [2^14, 2^15)
-                    c_r = p.sm_scale_log2 / qscale;
-                }
-            }
-#pragma unroll 1
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                uint32_t v[32];
-                if (row_ok) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint4 x = qrow[c0 / 4 + i];
-                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if (C::kQuant)
-                                v[4 * i + k] = pack_half2(bf16_bits_to_float(w[k] & 0xFFFFu) * qscale,
-                                                          __uint_as_float(w[k] & 0xFFFF0000u) * qscale);
-                            else
-                                v[4 * i + k] = w[k];
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-                tmem_st32(lane_tm + C::kQCol + c0, v);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kQReady));
-        }
+        const int pair_bar = 1 + quarter;
+        const uint32_t xmax = sbase + L.xchg;                 // [parity][half][128]
+        const uint32_t xsum = xmax + 2 * 2 * 128 * 4;          // [half][128]
+        const float c_r = p.sm_scale_log2 / q_prescale;  // score scale in log2 units
         float m_run = -INFINITY, l_run = 0.f;
         const int last_visible = it.L - T + t_r;  // bottom-right causal mask
-        const float *ring = reinterpret_cast<const float *>(smem + L.scale_ring);
+        const uint32_t ring = sbase + L.scale_ring;  // shared address of the scale ring
         for (int i = 0; i < ntiles; ++i) {
             const int b = i & 1;
             if (!mbar_wait(bar(kSFull + b), (i >> 1) & 1, kWaitNs)) { ok = false; break; }
             tc_fence_after();
             if (warp_active) {
-                const int key0 = it.k_begin + i * kTile;
-                uint32_t s[64];
-                tmem_ld32(lane_tm + C::kSCol + b * kTile, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_ld32(lane_tm + C::kSCol + b * kTile + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                const int key0 = it.k_begin + i * kTile + half * 32;  // first key of this half
+                uint32_t s[32];
+                tmem_ld32(lane_tm + C::kSCol + b * kTile + half * 32, s);
                 tmem_wait_ld();
-                const float *ks = ring + (i % kScaleRing) * 2 * kTile;
-                const float *vs = ks + kTile;
+                const uint32_t ks = ring + (i % kScaleRing) * 2 * kTile * 4 + half * 32 * 4;
+                const uint32_t vs = ks + kTile * 4;
                 // pages outside the pool (only checked when the pool size is
                 // known) were replaced by page 0 when loading: mask their keys
                 uint32_t bad_pages = 0;
                 if (p.num_pages > 0) {
 #pragma unroll
-                    for (int pg = 0; pg < kTile / VA_PAGE_SIZE; ++pg) {
+                    for (int pg = 0; pg < 2; ++pg) {
                         const int key = key0 + pg * VA_PAGE_SIZE;
                         if (key < it.k_end) {
                             const int page = bt[key / VA_PAGE_SIZE];
@@ -429,29 +499,55 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         }
                     }
                 }
-                const bool full = key0 + kTile <= it.k_end && key0 + kTile - 1 <= last_visible && row_ok &&
-                                  bad_pages == 0;
-                float x[64];
-                float mt = -INFINITY;
+                const bool full = row_ok && key0 + 32 <= it.k_end && key0 + 31 <= last_visible && bad_pages == 0;
+                // x = raw score * k_scale (masked keys -inf); 8 independent max chains
+                float mx[8];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    float v = __uint_as_float(s[j]);
-                    if (C::kQuant) v *= ks[j];
-                    if (!full) {
-                        const int key = key0 + j;
-                        const bool vis = row_ok && key < it.k_end && key <= last_visible &&
-                                         !((bad_pages >> (j / VA_PAGE_SIZE)) & 1u);
-                        v = vis ? v : -INFINITY;
+                for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+                if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        if (C::kQuant) {
+                            const float4 sc = lds_f4(ks + 16 * j4);
+                            s[4 * j4 + 0] = __float_as_uint(__uint_as_float(s[4 * j4 + 0]) * sc.x);
+                            s[4 * j4 + 1] = __float_as_uint(__uint_as_float(s[4 * j4 + 1]) * sc.y);
+                            s[4 * j4 + 2] = __float_as_uint(__uint_as_float(s[4 * j4 + 2]) * sc.z);
+                            s[4 * j4 + 3] = __float_as_uint(__uint_as_float(s[4 * j4 + 3]) * sc.w);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            mx[(4 * j4 + e) & 7] = fmaxf(mx[(4 * j4 + e) & 7], __uint_as_float(s[4 * j4 + e]));
                     }
-                    x[j] = v;
-                    mt = fmaxf(mt, v);
+                } else {
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float4 sc = make_float4(1.f, 1.f, 1.f, 1.f);
+                        if (C::kQuant) sc = lds_f4(ks + 16 * j4);
+                        const float scv[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * j4 + e;
+                            const int key = key0 + j;
+                            const bool vis = row_ok && key < it.k_end && key <= last_visible &&
+                                             !((bad_pages >> (j / VA_PAGE_SIZE)) & 1u);
+                            const float v = vis ? __uint_as_float(s[j]) * scv[e] : -INFINITY;
+                            s[j] = __float_as_uint(v);
+                            mx[j & 7] = fmaxf(mx[j & 7], v);
+                        }
+                    }
                 }
+                float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // exchange with the other half (double-buffered by tile parity)
+                sts_f32(xmax + 4u * ((b * 2 + half) * 128 + r), mt);
+                named_bar_sync(pair_bar, 64);
+                mt = fmaxf(mt, lds_f32(xmax + 4u * ((b * 2 + 1 - half) * 128 + r)));
                 const float m_tile = mt * c_r;  // -inf stays -inf (c_r > 0)
                 const bool grow = m_tile > m_run + kRescaleLog2;
                 const bool rescale = grow && m_run != -INFINITY;
                 float alpha = 1.f;
                 if (grow) {
-                    if (rescale) alpha = exp2f(m_run - m_tile);
+                    if (rescale) alpha = ex2_approx(m_run - m_tile);
                     m_run = m_tile;
                     l_run *= alpha;
                 }
@@ -460,7 +556,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     if (!mbar_wait(bar(kODone), (i - 1) & 1, kWaitNs)) { ok = false; }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                         uint32_t o[32];
                         tmem_ld32(lane_tm + C::kOCol + c0, o);
                         tmem_wait_ld();
@@ -470,25 +566,31 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     }
                     tmem_wait_st();
                 }
+                // p = 2^(x*c - m); masked keys give 2^-inf = 0 and carry a zero
+                // v scale, so no select is needed
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-                uint32_t pk[32];
-                float lsum = 0.f;
+                uint32_t pk[16];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (x[j] != -INFINITY) p0 = exp2f(fmaf(x[j], c_r, neg_m));
-                    if (x[j + 1] != -INFINITY) p1 = exp2f(fmaf(x[j + 1], c_r, neg_m));
-                    lsum += p0 + p1;
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 0]), c_r, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 1]), c_r, neg_m));
+                    const float p2 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 2]), c_r, neg_m));
+                    const float p3 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 3]), c_r, neg_m));
+                    ls[j4 & 3] += (p0 + p1) + (p2 + p3);
                     if (C::kQuant) {
-                        const float w0 = x[j] != -INFINITY ? p0 * vs[j] : 0.f;
-                        const float w1 = x[j + 1] != -INFINITY ? p1 * vs[j + 1] : 0.f;
-                        pk[j / 2] = pack_half2(w0, w1);
+                        const float4 sc = lds_f4(vs + 16 * j4);
+                        pk[2 * j4] = pack_half2(p0 * sc.x, p1 * sc.y);
+                        pk[2 * j4 + 1] = pack_half2(p2 * sc.z, p3 * sc.w);
                     } else {
-                        pk[j / 2] = pack_bf162(p0, p1);
+                        pk[2 * j4] = pack_bf162(p0, p1);
+                        pk[2 * j4 + 1] = pack_bf162(p2, p3);
                     }
                 }
-                l_run += lsum;
-                tmem_st32(lane_tm + C::kSCol + b * kTile, pk);
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                // P (16-bit, two keys per column) over S columns [16 half, 16 half + 16):
+                // both halves have read their S columns before the exchange above
+                tmem_st16(lane_tm + C::kSCol + b * kTile + half * 16, pk);
                 tmem_wait_st();
             }
             if (!C::kQuant && it.k_begin + i * kTile + kTile > it.k_end) {
@@ -498,12 +600,11 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 const int buf = i % C::kNumBuf;
                 if (!mbar_wait(bar(kVFull + buf), (i / C::kNumBuf) & 1, kWaitNs)) ok = false;
                 const int valid = it.k_end - key0;
-                unsigned char *vb = smem + L.conv_v + buf * C::kConvBytes;
-                const int qt = (warp - 2) * 32 + lane;  // 0..127 over the 4 softmax warps
-                for (int e = qt; e < (kTile - valid) * (D / 8); e += 128) {
+                const uint32_t vb = sbase + L.conv_v + buf * C::kConvBytes;
+                const int qt = warp * 32 + lane;  // 0..255 over the softmax warps
+                for (int e = qt; e < (kTile - valid) * (D / 8); e += C::kSoftmaxWarps * 32) {
                     const int row = valid + e / (D / 8), u16 = e % (D / 8);
-                    *reinterpret_cast<uint4 *>(vb + (u16 / 8) * C::kChunkBytes + sw128(row, u16 % 8)) =
-                        make_uint4(0, 0, 0, 0);
+                    sts_u4(vb + (u16 / 8) * C::kChunkBytes + sw128(row, u16 % 8), make_uint4(0, 0, 0, 0));
                 }
                 fence_proxy_async_smem();
             }
@@ -511,22 +612,25 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kPFull + b));
         }
-        // epilogue: O / l and the log-sum-exp
+        // epilogue: O / l and the log-sum-exp (the pair adds its partial sums)
         if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         tc_fence_after();
-        if (warp_active && ok) {
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        if (warp_active) {
+            sts_f32(xsum + 4u * (half * 128 + r), l_run);
+            named_bar_sync(pair_bar, 64);
+            const float l_tot = l_run + lds_f32(xsum + 4u * ((1 - half) * 128 + r));
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const float lse_nat = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
             const int rr = row0 + r;
             const int h = it.kvh * G + rr % G;
             const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + h;
             const size_t prow = (size_t)it.part * p.rows_per_group + r;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(lane_tm + C::kOCol + c0, o);
                 tmem_wait_ld();
-                if (!row_ok) continue;
+                if (!row_ok || !ok) continue;
                 if (it.part < 0) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c0);
 #pragma unroll
@@ -547,7 +651,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                                              __uint_as_float(o[4 * k + 3]) * inv);
                 }
             }
-            if (row_ok) {
+            if (row_ok && ok && half == 0) {
                 if (it.part < 0) {
                     if (p.lse) p.lse[orow] = lse_nat;
                 } else {
@@ -555,100 +659,100 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 }
             }
         }
-    } else if (C::kQuant) {
+    } else if constexpr (C::kQuant) {
         // ------------------------------------------------------------ dequant
-        const int dt = tid - 6 * 32;  // 0..127
-        const int dwarp = warp - 6;
-        float *ring = reinterpret_cast<float *>(smem + L.scale_ring);
-        constexpr int kChunks = kRawKeys * D / 16;  // 16-byte raw chunks per half tile
-        for (int i = 0; i < ntiles && ok; ++i) {
+        // One pass per raw stage: the K tile (plus this head's k and v scales,
+        // which the softmax of the tile needs) or the V tile, int8 / e4m3 ->
+        // fp16 (exact) into the MMA layout.
+        constexpr int kDT = C::kDequantWarps * 32;
+        const int dt = tid - C::kSoftmaxWarps * 32;  // 0 .. kDT-1
+        const uint32_t ring = sbase + L.scale_ring;
+        constexpr int kChunks = kTile * D / 16;      // 16-byte raw chunks per tile
+        constexpr int kPer = kChunks / kDT;          // per thread (1, 2 or 4)
+        static_assert(kPer * kDT == kChunks, "chunks must divide evenly");
+        // this thread's chunks: raw byte offset, tile row and destinations of
+        // its two 16-byte fp16 units (store order alternates between 64-d
+        // chunks so that a quarter-warp never hits a bank twice)
+        uint32_t roff[kPer], woff_lo[kPer], woff_hi[kPer];
+        int row_of[kPer];
+#pragma unroll
+        for (int jj = 0; jj < kPer; ++jj) {
+            const int q = dt + kDT * jj;
+            const int n = q * 16 / D, d0 = (q * 16) % D;
+            const int c = d0 / 64, u0 = (d0 % 64) / 8;
+            roff[jj] = q * 16;
+            row_of[jj] = n;
+            woff_lo[jj] = c * C::kChunkBytes + sw128(n, u0);
+            woff_hi[jj] = c * C::kChunkBytes + sw128(n, u0 + 1);
+        }
+        const bool odd_chunk = ((dt * 16 % D) / 64) & 1;  // same parity for every jj (kDT*16 % 128 == 0)
+        // threads dt < 128 carry one scale of the next tile: k (dt < 64) or v
+        // of key dt % 64, loaded from global a whole tile before it is needed
+        const float *scale_src = dt < kTile ? p.k_scale : p.v_scale;
+        auto load_scale = [&](int i) -> float {
+            const int n = dt % kTile;
+            const int key = it.k_begin + i * kTile + n;
+            if (dt >= 2 * kTile || i >= ntiles || key >= it.k_end) return 0.f;
+            const int page = (int)lds_u32(sbase + L.pids + 4u * (i * (kTile / VA_PAGE_SIZE) + n / VA_PAGE_SIZE));
+            return __ldg(scale_src + ((size_t)page * VA_PAGE_SIZE + n % VA_PAGE_SIZE) * Hkv + it.kvh);
+        };
+        float scale_cur = load_scale(0);
+        const int npass = 2 * ntiles;
+        for (int ps = 0; ps < npass && ok; ++ps) {
+            const int i = ps >> 1, kv = ps & 1;
             const int buf = i % C::kNumBuf, use = i / C::kNumBuf;
             const int key0 = it.k_begin + i * kTile;
-            float *ks_out = ring + (i % kScaleRing) * 2 * kTile;
-            float *vs_out = ks_out + kTile;
-#pragma unroll 1
-            for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int empty_bar = kv == 0 ? kKEmpty : kVEmpty;
-                if (!mbar_wait(bar(empty_bar + buf), (use & 1) ^ 1, kWaitNs)) { ok = false; break; }
-                unsigned char *dst = smem + (kv == 0 ? L.conv_k : L.conv_v) + buf * C::kConvBytes;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    const int rs = 2 * i + h;
-                    const int hkey0 = key0 + h * kRawKeys;
-                    const bool have = hkey0 < it.k_end;
-                    const int slot = rs % kRawStages;
-                    if (have && !mbar_wait(bar(kRawFull + slot), (rs / kRawStages) & 1, kWaitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    const unsigned char *st = smem + L.raw + slot * L.raw_stride;
-                    const unsigned char *src = st + (kv == 0 ? 0 : L.raw_v);
-#pragma unroll 2
-                    for (int q = dt; q < kChunks; q += 128) {
-                        const int n = q * 16 / D;            // key within the half tile
-                        const int d0 = (q * 16) % D;
-                        const int row = h * kRawKeys + n;    // key within the 64-key tile
-                        const int key = hkey0 + n;
-                        uint4 w = make_uint4(0, 0, 0, 0);
-                        if (have && key < it.k_end) {
-                            const uint4 raw = *reinterpret_cast<const uint4 *>(src + n * D + d0);
-                            const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-                            uint32_t hw[8];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                if (DT == VA_INT8)
-                                    int8x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
-                                else
-                                    e4m3x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
-                            }
-                            const int c = d0 / 64, u0 = (d0 % 64) / 8;
-                            const uint4 lo = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            const uint4 hi = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-                            unsigned char *cb = dst + c * C::kChunkBytes;
-                            if (c & 1) {  // alternate the store order between chunks: no bank conflicts
-                                *reinterpret_cast<uint4 *>(cb + sw128(row, u0 + 1)) = hi;
-                                *reinterpret_cast<uint4 *>(cb + sw128(row, u0)) = lo;
-                            } else {
-                                *reinterpret_cast<uint4 *>(cb + sw128(row, u0)) = lo;
-                                *reinterpret_cast<uint4 *>(cb + sw128(row, u0 + 1)) = hi;
-                            }
-                        } else {
-                            const int c = d0 / 64, u0 = (d0 % 64) / 8;
-                            unsigned char *cb = dst + c * C::kChunkBytes;
-                            *reinterpret_cast<uint4 *>(cb + sw128(row, u0)) = w;
-                            *reinterpret_cast<uint4 *>(cb + sw128(row, u0 + 1)) = w;
-                        }
-                    }
-                    // this head's k and v scales of the 32 keys, published
-                    // with K (the softmax of this tile needs both)
-                    if (kv == 0 && dt < 2 * kRawKeys) {
-                        const int n = dt % kRawKeys, which = dt / kRawKeys;
-                        const float *sc = reinterpret_cast<const float *>(st + (which == 0 ? L.raw_ks : L.raw_vs));
-                        float v = 0.f;
-                        if (have && hkey0 + n < it.k_end) v = sc[(n / VA_PAGE_SIZE) * VA_PAGE_SIZE * Hkv +
-                                                                 (n % VA_PAGE_SIZE) * Hkv + it.kvh];
-                        (which == 0 ? ks_out : vs_out)[h * kRawKeys + n] = v;
-                    }
-                }
-                if (!ok) break;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar((kv == 0 ? kKFull : kVFull) + buf));
+            const int nvalid = min(kTile, it.k_end - key0);
+            const int slot = ps % nst;
+            if (!mbar_wait(bar((kv == 0 ? kKEmpty : kVEmpty) + buf), (use & 1) ^ 1, kWaitNs) ||
+                !mbar_wait(bar(kRawFull + slot), (ps / nst) & 1, kWaitNs)) {
+                ok = false;
+                break;
             }
-            if (!ok) break;
-            // both K and V of the two raw stages have been read
+            const uint32_t st = sbase + L.raw + slot * L.raw_stride;
+            const uint32_t dst = sbase + (kv == 0 ? L.conv_k : L.conv_v) + buf * C::kConvBytes;
+            uint4 raw[kPer];
+#pragma unroll
+            for (int jj = 0; jj < kPer; ++jj) raw[jj] = lds_u4(st + roff[jj]);
+#pragma unroll
+            for (int jj = 0; jj < kPer; ++jj) {
+                uint32_t hw[8];
+                const uint32_t rw[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (DT == VA_INT8)
+                        int8x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
+                    else
+                        e4m3x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
+                }
+                uint4 lo = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                uint4 hi = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                if (row_of[jj] >= nvalid) lo = hi = make_uint4(0, 0, 0, 0);  // past the split end
+                if (odd_chunk) {
+                    sts_u4(dst + woff_hi[jj], hi);
+                    sts_u4(dst + woff_lo[jj], lo);
+                } else {
+                    sts_u4(dst + woff_lo[jj], lo);
+                    sts_u4(dst + woff_hi[jj], hi);
+                }
+            }
+            if (kv == 0) {  // the tile's k and v scales (zero past the end) -> ring; fetch the next tile's
+                if (dt < 2 * kTile) sts_f32(ring + (i % kScaleRing) * 2 * kTile * 4 + 4u * dt, scale_cur);
+                scale_cur = load_scale(i + 1);
+            }
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0)
-                for (int h = 0; h < 2; ++h)
-                    if (key0 + h * kRawKeys < it.k_end) mbar_arrive(bar(kRawEmpty + (2 * i + h) % kRawStages));
-            (void)dwarp;
+            if (lane == 0) {
+                mbar_arrive(bar((kv == 0 ? kKFull : kVFull) + buf));
+                mbar_arrive(bar(kRawEmpty + slot));
+            }
         }
     }
 
     if (!ok) atomicOr(p.flags, kFlagTimeout);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -700,8 +804,15 @@ cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
     if (!make_map(&mp.tm_k, p.k_pages, D, p.Hkv, p.num_pages, bf16) ||
         !make_map(&mp.tm_v, p.v_pages, D, p.Hkv, p.num_pages, bf16))
         return cudaErrorInvalidValue;
-    const Smem<D, DT> L(p.Hkv);
+    int nst = 0;
+    if (Cfg<D, DT>::kQuant) {
+        nst = kMaxRawStages;
+        while (nst > kMinRawStages && Smem<D, DT>(p.Hkv, nst).total + 1024 > kMaxSmemPerBlock) --nst;
+    }
+    mp.raw_stages = nst;
+    const Smem<D, DT> L(p.Hkv, nst);
     const size_t smem = L.total + 1024;  // + alignment slack
+    if (smem > kMaxSmemPerBlock) return cudaErrorInvalidConfiguration;
     auto k = mma_partial_kernel<D, DT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -720,14 +831,15 @@ cudaError_t launch_d(const PartialParams &p, int dtype, int n, cudaStream_t s) {
 
 }  // namespace
 
+// Shared memory of the tensor-core kernel with the fewest raw stages it runs
+// with (the planner falls back to the CUDA-core kernel when this exceeds the
+// per-block limit).
 size_t mma_smem_bytes(int head_dim, int kv_dtype, int Hkv) {
+    const bool bf = kv_dtype == VA_BF16;
     switch (head_dim) {
-    case 64:
-        return kv_dtype == VA_BF16 ? Smem<64, VA_BF16>(Hkv).total + 1024 : Smem<64, VA_INT8>(Hkv).total + 1024;
-    case 128:
-        return kv_dtype == VA_BF16 ? Smem<128, VA_BF16>(Hkv).total + 1024 : Smem<128, VA_INT8>(Hkv).total + 1024;
-    default:
-        return kv_dtype == VA_BF16 ? Smem<256, VA_BF16>(Hkv).total + 1024 : Smem<256, VA_INT8>(Hkv).total + 1024;
+    case 64: return (bf ? Smem<64, VA_BF16>(Hkv, 0).total : Smem<64, VA_INT8>(Hkv, kMinRawStages).total) + 1024;
+    case 128: return (bf ? Smem<128, VA_BF16>(Hkv, 0).total : Smem<128, VA_INT8>(Hkv, kMinRawStages).total) + 1024;
+    default: return (bf ? Smem<256, VA_BF16>(Hkv, 0).total : Smem<256, VA_INT8>(Hkv, kMinRawStages).total) + 1024;
     }
 }
 

@@ -41,6 +41,7 @@ struct va_plan {
 namespace {
 
 thread_local va_plan *t_current_plan = nullptr;
+thread_local int t_last_cuda_error = 0;
 
 struct Geometry {
     int path, rows_per_group, num_row_groups, tile, tokens_per_split, slots;
@@ -106,7 +107,7 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
 int choose_path(int R, int Hkv, const va_plan_options *opts) {
     int want = opts ? opts->path : VA_PATH_AUTO;
     if (want != VA_PATH_AUTO) return want;
-    return (R >= va::kMmaMinRows && Hkv <= va::kMmaMaxKvHeads) ? VA_PATH_MMA : VA_PATH_WARP;
+    return R >= va::kMmaMinRows ? VA_PATH_MMA : VA_PATH_WARP;
 }
 
 int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int dtype,
@@ -114,7 +115,11 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
     const int G = Hq / Hkv;
     const int R = G * T;
     g.path = choose_path(R, Hkv, opts);
-    if (g.path == VA_PATH_MMA && Hkv > va::kMmaMaxKvHeads) return VA_ERR_UNSUPPORTED;
+    if (g.path == VA_PATH_MMA && va::mma_smem_bytes(D, dtype, Hkv) > va::kMaxSmemPerBlock) {
+        // the page scale blocks of a large kv-head count do not fit next to the tiles
+        if (opts && opts->path == VA_PATH_MMA) return VA_ERR_UNSUPPORTED;
+        g.path = VA_PATH_WARP;
+    }
     const bool mma = g.path == VA_PATH_MMA;
     const int max_rows = mma ? va::kMmaRows : va::kWarpRows;
     g.tile = mma ? va::kMmaTile : va::kWarpTile;
@@ -153,9 +158,12 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
         return lpt_makespan(v, g.slots);
     };
 
+    // the tcgen05 kernel stages an item's page ids in shared memory
+    const int cap = mma ? va::kMmaMaxItemTokens : (1 << 30);
     int chosen;
     if (opts && opts->tokens_per_split > 0) {
         chosen = (opts->tokens_per_split + g.tile - 1) / g.tile * g.tile;
+        chosen = std::min(chosen, cap);
     } else {
         // Candidates: the one-wave length and a few multiples of the slot
         // count, plus "no split"; the smallest LPT makespan wins (ties go to
@@ -166,9 +174,9 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
             double c = units / (g.slots * waves);  // key tokens per item for `waves` items per slot
             int ci = (int)std::ceil(c / g.tile) * g.tile;
             ci = std::max(ci, 4 * g.tile);
-            cand.push_back(ci);
+            cand.push_back(std::min(ci, cap));
         }
-        cand.push_back(std::max(maxL, g.tile));
+        cand.push_back(std::min(std::max(maxL, g.tile), cap));
         std::sort(cand.begin(), cand.end());
         cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
         double best = 1e300;
@@ -259,7 +267,19 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+namespace va {
+void note_cuda_error(cudaError_t e) {
+    if (e != cudaSuccess) t_last_cuda_error = (int)e;
+}
+}  // namespace va
+
 extern "C" {
+
+int verify_attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *verify_attn_last_cuda_error_string(void) {
+    return cudaGetErrorString(static_cast<cudaError_t>(t_last_cuda_error));
+}
 
 const char *verify_attn_status_string(int status) {
     switch (status) {
@@ -480,6 +500,7 @@ int verify_attn_with_plan(const va_plan *p, const void *q, const void *k_pages,
                         ? va::launch_mma_partial(pp, p->D, p->kv_dtype, p->num_items, s)
                         : va::launch_warp_partial(pp, p->D, p->kv_dtype, p->num_items, s);
     if (e != cudaSuccess) {
+        va::note_cuda_error(e);
         cudaGetLastError();
         return VA_ERR_CUDA;
     }
@@ -499,7 +520,11 @@ int verify_attn_with_plan(const va_plan *p, const void *q, const void *k_pages,
         cp.rows_per_group = p->rows_per_group;
         cp.D = p->D;
         e = va::launch_combine(cp, p->num_groups, p->max_splits, s);
-        if (e != cudaSuccess) return VA_ERR_CUDA;
+        if (e != cudaSuccess) {
+            va::note_cuda_error(e);
+            cudaGetLastError();
+            return VA_ERR_CUDA;
+        }
     }
     return VA_OK;
 }
