@@ -57,6 +57,7 @@ constexpr int kBfStages = 3;        // bf16: 64-key stages TMA'd straight into M
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kScaleRing = 4;       // per-tile k/v scales handed to the softmax warps
+constexpr int kPTileBytes = 128 * kTile * 2;  // one P tile (A operand of P x V)
 constexpr int kMaxItemPages = kMmaMaxItemTokens / VA_PAGE_SIZE;  // page ids staged in smem
 
 enum : int { kFlagTimeout = 4 };
@@ -71,7 +72,7 @@ struct MmaParams {
 template <int D, int DT>
 struct Cfg {
     static constexpr bool kQuant = DT != VA_BF16;
-    static constexpr int kNumBuf = kQuant ? 2 : kBfStages;
+    static constexpr int kNumBuf = kQuant ? 2 : (D == 256 ? 2 : kBfStages);  // 64 KB bf16 stages at D = 256
     static constexpr int kConvBytes = kTile * D * 2;   // K or V tile, 16-bit, SW128 chunks of 64 d
     static constexpr int kChunkBytes = kTile * 128;    // one 64-d chunk of a tile
     static constexpr int kRawTileBytes = kTile * D;    // one K or V tile, 8-bit
@@ -96,6 +97,7 @@ template <int D, int DT>
 struct Smem {
     using C = Cfg<D, DT>;
     uint32_t conv_k, conv_v;         // kNumBuf buffers each
+    uint32_t pbuf;                   // 2 P tiles: 128 rows x 64 keys, 16-bit, SW128 K-major
     uint32_t raw, raw_stride;        // raw stages
     uint32_t pids;                   // the item's page ids (kMaxItemPages ints)
     uint32_t scale_ring;             // kScaleRing x (64 k + 64 v) floats
@@ -105,7 +107,8 @@ struct Smem {
     __host__ __device__ Smem(int Hkv, int nst) {
         conv_k = 0;
         conv_v = conv_k + C::kNumBuf * C::kConvBytes;
-        raw = conv_v + C::kNumBuf * C::kConvBytes;
+        pbuf = conv_v + C::kNumBuf * C::kConvBytes;
+        raw = pbuf + 2 * kPTileBytes;
         (void)Hkv;
         raw_stride = C::kQuant ? C::kRawTileBytes : 0;
         pids = raw + (C::kQuant ? nst * raw_stride : 0);
@@ -127,7 +130,8 @@ enum Bar : int {
     kSFull = kVEmpty + 3,               // 2
     kSFree = kSFull + 2,                // 2
     kPFull = kSFree + 2,                // 2
-    kODone = kPFull + 2,
+    kPEmpty = kPFull + 2,               // 2
+    kODone = kPEmpty + 2,
     kOFinal = kODone + 1,
     kQReady = kOFinal + 1,
     kNumBars = kQReady + 1,
@@ -215,9 +219,10 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             mbar_init(bar(kVEmpty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kSFull + i), 1);
-            mbar_init(bar(kSFree + i), 1);
-            mbar_init(bar(kPFull + i), C::kSoftmaxWarps);
+            mbar_init(bar(kSFull + i), 1);                    // QK^T committed
+            mbar_init(bar(kSFree + i), C::kSoftmaxWarps);     // softmax has read S
+            mbar_init(bar(kPFull + i), C::kSoftmaxWarps);     // softmax has written P
+            mbar_init(bar(kPEmpty + i), 1);                   // P x V committed
         }
         mbar_init(bar(kODone), 1);
         mbar_init(bar(kOFinal), 1);
@@ -416,12 +421,14 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         if (lane == 0) {
             constexpr int kAB = C::kQuant ? 0 : 1;  // fp16 (quantised caches) or bf16
             constexpr uint32_t idS = idesc_f16(128, kTile, kAB, 0, 0);
-            constexpr uint32_t idO = idesc_f16(128, D, kAB, 0, 1);
+            constexpr uint32_t idO = idesc_f16(128, D, kAB, 0, 1);  // A = P (K-major smem), B = V (MN-major)
             const uint32_t s_tm = tmem + C::kSCol, o_tm = tmem + C::kOCol, q_tm = tmem + C::kQCol;
             // K tile: K-major (d contiguous) SW128, 8-row groups 1024 B apart.
             // V tile: MN-major (d contiguous) SW128, 64-d chunks kChunkBytes apart.
             const uint64_t kdesc0 = smem_desc(sbase + L.conv_k, 16, 1024, 2);
             const uint64_t vdesc0 = smem_desc(sbase + L.conv_v, C::kChunkBytes, 1024, 2);
+            // P tile: 128 rows of 128 bytes (64 keys), SW128 K-major, 8-row groups 1024 B apart
+            const uint64_t pdesc0 = smem_desc(sbase + L.pbuf, 16, 1024, 2);
             constexpr uint32_t kBufStep = C::kConvBytes >> 4;
             ok = mbar_wait(bar(kQReady), 0, kWaitNs);
             auto issue_pv = [&](int j) -> bool {
@@ -430,12 +437,13 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 if (!mbar_wait(bar(kVFull + buf), use & 1, kWaitNs)) return false;
                 tc_fence_after();
                 const uint64_t vd = vdesc0 + (uint64_t)(buf * kBufStep);
+                const uint64_t pd = pdesc0 + (uint64_t)(b * (kPTileBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(o_tm, s_tm + b * kTile + kk * 8, vd + (uint64_t)(kk * (16 * 128 >> 4)), idO,
+                    mma_ss(o_tm, pd + (uint64_t)(kk * 2), vd + (uint64_t)(kk * (16 * 128 >> 4)), idO,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(kVEmpty + buf));
-                mma_commit(bar(kSFree + b));
+                mma_commit(bar(kPEmpty + b));
                 mma_commit(bar(kODone));
                 return true;
             };
@@ -479,11 +487,18 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             const int b = i & 1;
             if (!mbar_wait(bar(kSFull + b), (i >> 1) & 1, kWaitNs)) { ok = false; break; }
             tc_fence_after();
-            if (warp_active) {
+            if (!warp_active) {  // all rows of this quarter are padding: only release S
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kSFree + b));
+            } else {
                 const int key0 = it.k_begin + i * kTile + half * 32;  // first key of this half
                 uint32_t s[32];
                 tmem_ld32(lane_tm + C::kSCol + b * kTile + half * 32, s);
                 tmem_wait_ld();
+                // S is in registers: the buffer may take QK^T of tile i + 2
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kSFree + b));
                 const uint32_t ks = ring + (i % kScaleRing) * 2 * kTile * 4 + half * 32 * 4;
                 const uint32_t vs = ks + kTile * 4;
                 // pages outside the pool (only checked when the pool size is
@@ -553,7 +568,8 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 }
                 if (__any_sync(0xffffffffu, rescale) && i > 0) {
                     // O holds the earlier tiles: wait until PV(i-1) has landed
-                    if (!mbar_wait(bar(kODone), (i - 1) & 1, kWaitNs)) { ok = false; }
+                    // (its commit completes the ((i-1)/2)-th phase of P buffer (i-1)%2)
+                    if (!mbar_wait(bar(kPEmpty + ((i - 1) & 1)), ((i - 1) >> 1) & 1, kWaitNs)) { ok = false; }
                     tc_fence_after();
 #pragma unroll 1
                     for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
@@ -588,10 +604,15 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     }
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                // P (16-bit, two keys per column) over S columns [16 half, 16 half + 16):
-                // both halves have read their S columns before the exchange above
-                tmem_st16(lane_tm + C::kSCol + b * kTile + half * 16, pk);
-                tmem_wait_st();
+                // P row r, keys [32 half, 32 half + 32): 16-byte units 4 half .. 4 half + 3
+                // of the row's 128-byte swizzled line, once P x V of tile i - 2 is done
+                if (!mbar_wait(bar(kPEmpty + b), ((i >> 1) & 1) ^ 1, kWaitNs)) ok = false;
+                const uint32_t prow = sbase + L.pbuf + b * kPTileBytes + r * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    sts_u4(prow + (((4 * half + u) ^ (r & 7)) << 4),
+                           make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+                fence_proxy_async_smem();
             }
             if (!C::kQuant && it.k_begin + i * kTile + kTile > it.k_end) {
                 // last tile of the item: rows past the split end hold whatever
@@ -612,27 +633,33 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kPFull + b));
         }
-        // epilogue: O / l and the log-sum-exp (the pair adds its partial sums)
+        // epilogue: O / l and the log-sum-exp (the pair adds its partial sums).
+        // Each row's normalised output is staged in the tile buffers (free once
+        // the last P x V has completed), 16-byte units XOR-swizzled by row so
+        // that neither the row-per-thread writes nor the reads conflict, then
+        // all softmax threads copy the item's rows out with consecutive
+        // 16-byte stores: fp32 into the split partials, or bf16 into out for
+        // an unsplit item.
         if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         tc_fence_after();
+        const bool final_out = it.part < 0;
+        const int cb = final_out ? D / 8 : D / 4;  // 16-byte units per staged row
+        const uint32_t stage = sbase + L.conv_k;
+        auto unit = [](int row, int c) { return (uint32_t)(((c & ~7) | ((c ^ row) & 7)) << 4); };
         if (warp_active) {
             sts_f32(xsum + 4u * (half * 128 + r), l_run);
             named_bar_sync(pair_bar, 64);
             const float l_tot = l_run + lds_f32(xsum + 4u * ((1 - half) * 128 + r));
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const float lse_nat = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
-            const int rr = row0 + r;
-            const int h = it.kvh * G + rr % G;
-            const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + h;
-            const size_t prow = (size_t)it.part * p.rows_per_group + r;
+            const uint32_t srow = stage + (uint32_t)(r * cb * 16);
 #pragma unroll 1
             for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(lane_tm + C::kOCol + c0, o);
                 tmem_wait_ld();
-                if (!row_ok || !ok) continue;
-                if (it.part < 0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c0);
+                if (!row_ok) continue;
+                if (final_out) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint4 w;
@@ -640,22 +667,45 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         w.y = pack_bf162(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
                         w.z = pack_bf162(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
                         w.w = pack_bf162(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-                        dst[k] = w;
+                        sts_u4(srow + unit(r, c0 / 8 + k), w);
                     }
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D + c0);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv,
-                                             __uint_as_float(o[4 * k + 3]) * inv);
+                        sts_u4(srow + unit(r, c0 / 4 + k),
+                               make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
+                    // (scaled below, on the way out)
                 }
             }
-            if (row_ok && ok && half == 0) {
-                if (it.part < 0) {
-                    if (p.lse) p.lse[orow] = lse_nat;
+            if (row_ok && half == 0) {
+                // the row's 1/l for the copy-out, and its log-sum-exp
+                sts_f32(xsum + 4u * (128 + r), inv);
+                if (ok) {
+                    const int rr = row0 + r;
+                    const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + it.kvh * G + rr % G;
+                    if (final_out) {
+                        if (p.lse) p.lse[orow] = lse_nat;
+                    } else {
+                        p.lse_part[(size_t)it.part * p.rows_per_group + r] = lse_nat;
+                    }
+                }
+            }
+        }
+        named_bar_sync(9, C::kSoftmaxWarps * 32);  // all rows staged
+        if (ok) {
+            const int st = warp * 32 + lane;  // 0 .. 255
+            for (int e = st; e < nrows * cb; e += C::kSoftmaxWarps * 32) {
+                const int row = e / cb, c = e % cb;
+                uint4 v = lds_u4(stage + (uint32_t)(row * cb * 16) + unit(row, c));
+                if (final_out) {
+                    const int rr = row0 + row;
+                    const size_t orow = (size_t)(it.b * T + rr / G) * p.Hq + it.kvh * G + rr % G;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.out) + orow * D * 2 + c * 16) = v;
                 } else {
-                    p.lse_part[prow] = lse_nat;
+                    const float inv = lds_f32(xsum + 4u * (128 + row));
+                    const float4 f = make_float4(__uint_as_float(v.x) * inv, __uint_as_float(v.y) * inv,
+                                                 __uint_as_float(v.z) * inv, __uint_as_float(v.w) * inv);
+                    *reinterpret_cast<float4 *>(p.o_part + ((size_t)it.part * p.rows_per_group + row) * D + c * 4) = f;
                 }
             }
         }
