@@ -40,6 +40,7 @@ struct PartialParams {
     float *lse_part;            // [num_parts, rows_per_group]
     int *flags;
     int bt_stride, T, Hq, Hkv, G, R, rows_per_group, num_pages;
+    int num_parts;              // split partials in o_part / lse_part
     float sm_scale_log2;        // log2(e) / sqrt(D)
 };
 

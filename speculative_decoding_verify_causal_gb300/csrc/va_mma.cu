@@ -40,6 +40,7 @@
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "va_internal.h"
@@ -57,14 +58,15 @@ constexpr int kBfStages = 3;        // bf16: 64-key stages TMA'd straight into M
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kScaleRing = 4;       // per-tile k/v scales handed to the softmax warps
-constexpr int kPTileBytes = 128 * kTile * 2;  // one P tile (A operand of P x V)
 constexpr int kMaxItemPages = kMmaMaxItemTokens / VA_PAGE_SIZE;  // page ids staged in smem
+constexpr int kSetupBar = 10;       // named barrier: set-up done (producer arrives, the rest wait)
 
 enum : int { kFlagTimeout = 4 };
 
 struct MmaParams {
     CUtensorMap tm_k;  // 64-byte aligned members first
     CUtensorMap tm_v;
+    CUtensorMap tm_o;  // split partials o_part as [num_parts * rows_per_group, D] fp32 (unused if none)
     PartialParams p;
     int raw_stages;    // quantised caches: stages of the raw ring (fits the smem budget)
 };
@@ -97,7 +99,6 @@ template <int D, int DT>
 struct Smem {
     using C = Cfg<D, DT>;
     uint32_t conv_k, conv_v;         // kNumBuf buffers each
-    uint32_t pbuf;                   // 2 P tiles: 128 rows x 64 keys, 16-bit, SW128 K-major
     uint32_t raw, raw_stride;        // raw stages
     uint32_t pids;                   // the item's page ids (kMaxItemPages ints)
     uint32_t scale_ring;             // kScaleRing x (64 k + 64 v) floats
@@ -107,8 +108,7 @@ struct Smem {
     __host__ __device__ Smem(int Hkv, int nst) {
         conv_k = 0;
         conv_v = conv_k + C::kNumBuf * C::kConvBytes;
-        pbuf = conv_v + C::kNumBuf * C::kConvBytes;
-        raw = pbuf + 2 * kPTileBytes;
+        raw = conv_v + C::kNumBuf * C::kConvBytes;
         (void)Hkv;
         raw_stride = C::kQuant ? C::kRawTileBytes : 0;
         pids = raw + (C::kQuant ? nst * raw_stride : 0);
@@ -128,14 +128,16 @@ enum Bar : int {
     kVFull = kKEmpty + 3,
     kVEmpty = kVFull + 3,
     kSFull = kVEmpty + 3,               // 2
-    kSFree = kSFull + 2,                // 2
-    kPFull = kSFree + 2,                // 2
+    kPFull = kSFull + 2,                // 2
     kPEmpty = kPFull + 2,               // 2
     kODone = kPEmpty + 2,
     kOFinal = kODone + 1,
     kQReady = kOFinal + 1,
-    kNumBars = kQReady + 1,
+    kRingFree = kQReady + 1,            // kScaleRing: the softmax has read a tile's scales
+    kNumBars = kRingFree + kScaleRing,
 };
+
+static_assert(kNumBars <= 64, "the barrier block holds 64 mbarriers");
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
@@ -187,6 +189,7 @@ template <int D, int DT>
 __global__ void __launch_bounds__(Cfg<D, DT>::kThreads, 1)
 mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     using C = Cfg<D, DT>;
+    static_assert(2 * C::kNumBuf * C::kConvBytes >= (D / 32) * kMmaRows * 128, "fp32 staging fits the tile buffers");
     const PartialParams &p = mp.p;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -207,30 +210,60 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     const int ntiles = (nkeys + kTile - 1) / kTile;
     const int32_t *bt = p.block_table + (size_t)it.b * p.bt_stride;
 
-    if (tid == 0) {
-        for (int i = 0; i < kMaxRawStages; ++i) {
-            mbar_init(bar(kRawFull + i), 1);
-            mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps : 1);
+    const int lp0 = it.k_begin / VA_PAGE_SIZE;                               // first logical page
+    const int npages_item = (it.k_end + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE - lp0;
+    if (warp == C::kProducerWarp) {
+        // Set-up by the producer warp, which then arrives at the set-up
+        // barrier without waiting for the others: its first copies go out
+        // while the other warps load Q and allocate TMEM.
+        if (lane == 0) {
+            for (int i = 0; i < kMaxRawStages; ++i) {
+                mbar_init(bar(kRawFull + i), 1);
+                mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps : 1);
+            }
+            for (int i = 0; i < 3; ++i) {
+                mbar_init(bar(kKFull + i), C::kQuant ? C::kDequantWarps : 1);
+                mbar_init(bar(kVFull + i), C::kQuant ? C::kDequantWarps : 1);
+                mbar_init(bar(kKEmpty + i), 1);
+                mbar_init(bar(kVEmpty + i), 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(bar(kSFull + i), 1);                    // QK^T committed
+                    mbar_init(bar(kPFull + i), C::kSoftmaxWarps);     // softmax has written P
+                mbar_init(bar(kPEmpty + i), 1);                   // P x V done: S/P buffer free
+            }
+            mbar_init(bar(kODone), 1);
+            mbar_init(bar(kOFinal), 1);
+            mbar_init(bar(kQReady), C::kSoftmaxWarps + C::kDequantWarps);
+            for (int i = 0; i < kScaleRing; ++i) mbar_init(bar(kRingFree + i), C::kSoftmaxWarps);
+            fence_barrier_init();
+            if (p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);
+            prefetch_tensormap(&mp.tm_k);
+            prefetch_tensormap(&mp.tm_v);
         }
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(bar(kKFull + i), C::kQuant ? C::kDequantWarps : 1);
-            mbar_init(bar(kVFull + i), C::kQuant ? C::kDequantWarps : 1);
-            mbar_init(bar(kKEmpty + i), 1);
-            mbar_init(bar(kVEmpty + i), 1);
+        // the item's page ids -> smem (bad entries replaced by page 0 and
+        // flagged); four loads per lane in flight at a time
+        for (int k0 = 0; k0 < npages_item; k0 += 128) {
+            int pg[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + 32 * j + lane;
+                pg[j] = k < npages_item ? __ldg(bt + lp0 + k) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + 32 * j + lane;
+                if (k >= npages_item) continue;
+                if (p.num_pages > 0 && (pg[j] < 0 || pg[j] >= p.num_pages)) {
+                    atomicOr(p.flags, kFlagBadPage);
+                    pg[j] = 0;
+                }
+                sts_u32(sbase + L.pids + 4u * k, (uint32_t)pg[j]);
+            }
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kSFull + i), 1);                    // QK^T committed
-            mbar_init(bar(kSFree + i), C::kSoftmaxWarps);     // softmax has read S
-            mbar_init(bar(kPFull + i), C::kSoftmaxWarps);     // softmax has written P
-            mbar_init(bar(kPEmpty + i), 1);                   // P x V committed
-        }
-        mbar_init(bar(kODone), 1);
-        mbar_init(bar(kOFinal), 1);
-        mbar_init(bar(kQReady), C::kSoftmaxWarps + C::kDequantWarps);
-        fence_barrier_init();
-        if (p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);
-    }
-    if (warp == C::kMmaWarp) {
+        __syncwarp();
+        named_bar_arrive(kSetupBar, C::kThreads);
+    } else if (warp == C::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -259,23 +292,12 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             for (int k = 0; k < kQv; ++k) qv[k] = make_uint4(0, 0, 0, 0);
         }
     }
-    const int lp0 = it.k_begin / VA_PAGE_SIZE;                               // first logical page
-    const int npages_item = (it.k_end + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE - lp0;
-    if (warp == C::kProducerWarp) {
-        // the item's page ids -> smem (bad entries replaced by page 0 and flagged)
-        for (int k = lane; k < npages_item; k += 32) {
-            int page = bt[lp0 + k];
-            if (p.num_pages > 0 && (page < 0 || page >= p.num_pages)) {
-                atomicOr(p.flags, kFlagBadPage);
-                page = 0;
-            }
-            sts_u32(sbase + L.pids + 4u * k, (uint32_t)page);
-        }
+    if (warp != C::kProducerWarp) {
+        tc_fence_before();
+        named_bar_sync(kSetupBar, C::kThreads);
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = warp == C::kProducerWarp ? 0u : *tmem_slot;
     bool ok = true;
     float q_prescale = 1.f;  // power of two folded into fp16 q (quantised caches)
     if (q_warp) {
@@ -340,10 +362,6 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the stages; lane pg issues the TMA box of the
         // tile's page pg (page ids come from smem, staged at kernel start).
-        if (lane == 0) {
-            prefetch_tensormap(&mp.tm_k);
-            prefetch_tensormap(&mp.tm_v);
-        }
         auto tile_page = [&](int i) -> int {  // lane pg: page pg of tile i (0 past the end)
             const int k = i * (kTile / VA_PAGE_SIZE) + lane;
             return (lane < kTile / VA_PAGE_SIZE && k < npages_item) ? (int)lds_u32(sbase + L.pids + 4u * k) : 0;
@@ -421,14 +439,12 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         if (lane == 0) {
             constexpr int kAB = C::kQuant ? 0 : 1;  // fp16 (quantised caches) or bf16
             constexpr uint32_t idS = idesc_f16(128, kTile, kAB, 0, 0);
-            constexpr uint32_t idO = idesc_f16(128, D, kAB, 0, 1);  // A = P (K-major smem), B = V (MN-major)
+            constexpr uint32_t idO = idesc_f16(128, D, kAB, 0, 1);  // A = P (TMEM), B = V (MN-major)
             const uint32_t s_tm = tmem + C::kSCol, o_tm = tmem + C::kOCol, q_tm = tmem + C::kQCol;
             // K tile: K-major (d contiguous) SW128, 8-row groups 1024 B apart.
             // V tile: MN-major (d contiguous) SW128, 64-d chunks kChunkBytes apart.
             const uint64_t kdesc0 = smem_desc(sbase + L.conv_k, 16, 1024, 2);
             const uint64_t vdesc0 = smem_desc(sbase + L.conv_v, C::kChunkBytes, 1024, 2);
-            // P tile: 128 rows of 128 bytes (64 keys), SW128 K-major, 8-row groups 1024 B apart
-            const uint64_t pdesc0 = smem_desc(sbase + L.pbuf, 16, 1024, 2);
             constexpr uint32_t kBufStep = C::kConvBytes >> 4;
             ok = mbar_wait(bar(kQReady), 0, kWaitNs);
             auto issue_pv = [&](int j) -> bool {
@@ -437,10 +453,10 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 if (!mbar_wait(bar(kVFull + buf), use & 1, kWaitNs)) return false;
                 tc_fence_after();
                 const uint64_t vd = vdesc0 + (uint64_t)(buf * kBufStep);
-                const uint64_t pd = pdesc0 + (uint64_t)(b * (kPTileBytes >> 4));
+                // P of tile j: fp16 pairs in the first kTile / 2 columns of S buffer b
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ss(o_tm, pd + (uint64_t)(kk * 2), vd + (uint64_t)(kk * (16 * 128 >> 4)), idO,
+                    mma_ts(o_tm, s_tm + b * kTile + kk * 8, vd + (uint64_t)(kk * (16 * 128 >> 4)), idO,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(kVEmpty + buf));
                 mma_commit(bar(kPEmpty + b));
@@ -449,8 +465,9 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             };
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int b = i & 1, buf = i % C::kNumBuf, use = i / C::kNumBuf;
+                // S buffer b holds P of tile i - 2 until that P x V has completed
                 if (!mbar_wait(bar(kKFull + buf), use & 1, kWaitNs) ||
-                    !mbar_wait(bar(kSFree + b), ((i >> 1) & 1) ^ 1, kWaitNs)) { ok = false; break; }
+                    !mbar_wait(bar(kPEmpty + b), ((i >> 1) & 1) ^ 1, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t kd = kdesc0 + (uint64_t)(buf * kBufStep);
 #pragma unroll
@@ -487,18 +504,14 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             const int b = i & 1;
             if (!mbar_wait(bar(kSFull + b), (i >> 1) & 1, kWaitNs)) { ok = false; break; }
             tc_fence_after();
-            if (!warp_active) {  // all rows of this quarter are padding: only release S
+            if (!warp_active) {  // all rows of this quarter are padding: only release the scales
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kSFree + b));
+                if (lane == 0) mbar_arrive(bar(kRingFree + i % kScaleRing));
             } else {
                 const int key0 = it.k_begin + i * kTile + half * 32;  // first key of this half
                 uint32_t s[32];
                 tmem_ld32(lane_tm + C::kSCol + b * kTile + half * 32, s);
                 tmem_wait_ld();
-                // S is in registers: the buffer may take QK^T of tile i + 2
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kSFree + b));
                 const uint32_t ks = ring + (i % kScaleRing) * 2 * kTile * 4 + half * 32 * 4;
                 const uint32_t vs = ks + kTile * 4;
                 // pages outside the pool (only checked when the pool size is
@@ -604,15 +617,13 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     }
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                // P row r, keys [32 half, 32 half + 32): 16-byte units 4 half .. 4 half + 3
-                // of the row's 128-byte swizzled line, once P x V of tile i - 2 is done
-                if (!mbar_wait(bar(kPEmpty + b), ((i >> 1) & 1) ^ 1, kWaitNs)) ok = false;
-                const uint32_t prow = sbase + L.pbuf + b * kPTileBytes + r * 128;
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    sts_u4(prow + (((4 * half + u) ^ (r & 7)) << 4),
-                           make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
-                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kRingFree + i % kScaleRing));  // scale slot read
+                // P row r, keys [32 half, 32 half + 32) -> columns [16 half, 16 half + 16)
+                // of S buffer b (the pair has read both halves of S: they met at
+                // the max exchange above)
+                tmem_st16(lane_tm + C::kSCol + b * kTile + half * 16, pk);
+                tmem_wait_st();
             }
             if (!C::kQuant && it.k_begin + i * kTile + kTile > it.k_end) {
                 // last tile of the item: rows past the split end hold whatever
@@ -643,8 +654,11 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         tc_fence_after();
         const bool final_out = it.part < 0;
-        const int cb = final_out ? D / 8 : D / 4;  // 16-byte units per staged row
+        const int cb = D / 8;  // 16-byte units per staged bf16 row
         const uint32_t stage = sbase + L.conv_k;
+        // fp32 partials: 32-column (128-byte) chunks, each the box of the
+        // partials' tensor map (rows padded to 8 keep every box 1024-byte aligned)
+        const uint32_t cstride = (uint32_t)((p.rows_per_group + 7) / 8 * 8) * 128u;
         auto unit = [](int row, int c) { return (uint32_t)(((c & ~7) | ((c ^ row) & 7)) << 4); };
         if (warp_active) {
             sts_f32(xsum + 4u * (half * 128 + r), l_run);
@@ -670,16 +684,21 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         sts_u4(srow + unit(r, c0 / 8 + k), w);
                     }
                 } else {
+                    // row r of chunk c0 / 32, 16-byte units XOR-swizzled by r % 8
+                    // (the tensor map's 128-byte swizzle; also conflict-free here)
+                    const uint32_t crow = stage + (uint32_t)(c0 / 32) * cstride + (uint32_t)r * 128u;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        sts_u4(srow + unit(r, c0 / 4 + k),
-                               make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
-                    // (scaled below, on the way out)
+                        sts_u4(crow + ((k ^ (r & 7)) << 4),
+                               make_uint4(__float_as_uint(__uint_as_float(o[4 * k]) * inv),
+                                          __float_as_uint(__uint_as_float(o[4 * k + 1]) * inv),
+                                          __float_as_uint(__uint_as_float(o[4 * k + 2]) * inv),
+                                          __float_as_uint(__uint_as_float(o[4 * k + 3]) * inv)));
                 }
             }
+            if (!final_out) fence_proxy_async_smem();  // staged rows -> the TMA store
             if (row_ok && half == 0) {
-                // the row's 1/l for the copy-out, and its log-sum-exp
-                sts_f32(xsum + 4u * (128 + r), inv);
+                // the row's log-sum-exp
                 if (ok) {
                     const int rr = row0 + r;
                     const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + it.kvh * G + rr % G;
@@ -692,22 +711,22 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             }
         }
         named_bar_sync(9, C::kSoftmaxWarps * 32);  // all rows staged
-        if (ok) {
+        if (ok && final_out) {
             const int st = warp * 32 + lane;  // 0 .. 255
             for (int e = st; e < nrows * cb; e += C::kSoftmaxWarps * 32) {
                 const int row = e / cb, c = e % cb;
-                uint4 v = lds_u4(stage + (uint32_t)(row * cb * 16) + unit(row, c));
-                if (final_out) {
-                    const int rr = row0 + row;
-                    const size_t orow = (size_t)(it.b * T + rr / G) * p.Hq + it.kvh * G + rr % G;
-                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.out) + orow * D * 2 + c * 16) = v;
-                } else {
-                    const float inv = lds_f32(xsum + 4u * (128 + row));
-                    const float4 f = make_float4(__uint_as_float(v.x) * inv, __uint_as_float(v.y) * inv,
-                                                 __uint_as_float(v.z) * inv, __uint_as_float(v.w) * inv);
-                    *reinterpret_cast<float4 *>(p.o_part + ((size_t)it.part * p.rows_per_group + row) * D + c * 4) = f;
-                }
+                const uint4 v = lds_u4(stage + (uint32_t)(row * cb * 16) + unit(row, c));
+                const int rr = row0 + row;
+                const size_t orow = (size_t)(it.b * T + rr / G) * p.Hq + it.kvh * G + rr % G;
+                *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.out) + orow * D * 2 + c * 16) = v;
             }
+        } else if (ok && warp == 0 && lane == 0) {
+            // the item's block of partials (rows past nrows are padding that
+            // nothing reads) leaves in D / 32 box stores
+            for (int k = 0; k < D / 32; ++k)
+                tma_store_2d(&mp.tm_o, k * 32, it.part * p.rows_per_group, stage + (uint32_t)k * cstride);
+            bulk_commit_group();
+            bulk_wait_group_read0();  // shared memory stays valid until the stores have read it
         }
     } else if constexpr (C::kQuant) {
         // ------------------------------------------------------------ dequant
@@ -736,8 +755,8 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             woff_hi[jj] = c * C::kChunkBytes + sw128(n, u0 + 1);
         }
         const bool odd_chunk = ((dt * 16 % D) / 64) & 1;  // same parity for every jj (kDT*16 % 128 == 0)
-        // threads dt < 128 carry one scale of the next tile: k (dt < 64) or v
-        // of key dt % 64, loaded from global a whole tile before it is needed
+        // threads dt < 128 carry one scale of a tile: k (dt < 64) or v of key
+        // dt % 64, loaded from global two tiles before it is needed
         const float *scale_src = dt < kTile ? p.k_scale : p.v_scale;
         auto load_scale = [&](int i) -> float {
             const int n = dt % kTile;
@@ -746,7 +765,9 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             const int page = (int)lds_u32(sbase + L.pids + 4u * (i * (kTile / VA_PAGE_SIZE) + n / VA_PAGE_SIZE));
             return __ldg(scale_src + ((size_t)page * VA_PAGE_SIZE + n % VA_PAGE_SIZE) * Hkv + it.kvh);
         };
-        float scale_cur = load_scale(0);
+        // two tiles of scales in flight: a global load under load takes about as
+        // long as a tile
+        float scale_cur = load_scale(0), scale_nxt = load_scale(1);
         const int npass = 2 * ntiles;
         for (int ps = 0; ps < npass && ok; ++ps) {
             const int i = ps >> 1, kv = ps & 1;
@@ -754,8 +775,9 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             const int key0 = it.k_begin + i * kTile;
             const int nvalid = min(kTile, it.k_end - key0);
             const int slot = ps % nst;
-            if (!mbar_wait(bar((kv == 0 ? kKEmpty : kVEmpty) + buf), (use & 1) ^ 1, kWaitNs) ||
-                !mbar_wait(bar(kRawFull + slot), (ps / nst) & 1, kWaitNs)) {
+            // the raw bytes go to registers and the stage is handed back to
+            // the producer at once, before waiting for the fp16 buffer
+            if (!mbar_wait(bar(kRawFull + slot), (ps / nst) & 1, kWaitNs)) {
                 ok = false;
                 break;
             }
@@ -764,6 +786,21 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             uint4 raw[kPer];
 #pragma unroll
             for (int jj = 0; jj < kPer; ++jj) raw[jj] = lds_u4(st + roff[jj]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kRawEmpty + slot));
+            // K pass: the tile's scales move up the pipeline and the load two
+            // tiles ahead is issued now, before this pass's stores fill the
+            // shared-memory queue
+            float scale_out = 0.f;
+            if (kv == 0) {
+                scale_out = scale_cur;
+                scale_cur = scale_nxt;
+                scale_nxt = load_scale(i + 2);
+            }
+            if (!mbar_wait(bar((kv == 0 ? kKEmpty : kVEmpty) + buf), (use & 1) ^ 1, kWaitNs)) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int jj = 0; jj < kPer; ++jj) {
                 uint32_t hw[8];
@@ -786,16 +823,14 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     sts_u4(dst + woff_hi[jj], hi);
                 }
             }
-            if (kv == 0) {  // the tile's k and v scales (zero past the end) -> ring; fetch the next tile's
-                if (dt < 2 * kTile) sts_f32(ring + (i % kScaleRing) * 2 * kTile * 4 + 4u * dt, scale_cur);
-                scale_cur = load_scale(i + 1);
+            if (kv == 0 && dt < 2 * kTile) {  // the tile's k and v scales (zero past the end) -> ring
+                // slot i % kScaleRing held tile i - kScaleRing, whose softmax has to have read it
+                if (!mbar_wait(bar(kRingFree + i % kScaleRing), ((i / kScaleRing) & 1) ^ 1, kWaitNs)) ok = false;
+                sts_f32(ring + (i % kScaleRing) * 2 * kTile * 4 + 4u * dt, scale_out);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar((kv == 0 ? kKFull : kVFull) + buf));
-                mbar_arrive(bar(kRawEmpty + slot));
-            }
+            if (lane == 0) mbar_arrive(bar((kv == 0 ? kKFull : kVFull) + buf));
         }
     }
 
@@ -829,6 +864,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// The split partials [num_parts * rows_per_group, D] fp32 as boxes of 32
+// columns x rows_per_group rows, 128-byte swizzled in shared memory.
+bool make_part_map(CUtensorMap *m, float *o_part, int D, int rows_per_group, int num_parts) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_parts * rows_per_group};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    cuuint32_t box[2] = {32u, (cuuint32_t)rows_per_group};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, o_part, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 4-D view of a page pool [pages, 16, Hkv, D]: dims innermost first.
 bool make_map(CUtensorMap *m, const void *base, int D, int Hkv, int num_pages, bool bf16) {
     EncodeTiledFn enc = encode_fn();
@@ -853,6 +903,9 @@ cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
     const bool bf16 = DT == VA_BF16;
     if (!make_map(&mp.tm_k, p.k_pages, D, p.Hkv, p.num_pages, bf16) ||
         !make_map(&mp.tm_v, p.v_pages, D, p.Hkv, p.num_pages, bf16))
+        return cudaErrorInvalidValue;
+    memset(&mp.tm_o, 0, sizeof(mp.tm_o));
+    if (p.num_parts > 0 && !make_part_map(&mp.tm_o, p.o_part, D, p.rows_per_group, p.num_parts))
         return cudaErrorInvalidValue;
     int nst = 0;
     if (Cfg<D, DT>::kQuant) {

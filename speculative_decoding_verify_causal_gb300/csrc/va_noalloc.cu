@@ -214,6 +214,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     pp.R = R;
     pp.rows_per_group = L.rows_per_group;
     pp.num_pages = 0;
+    pp.num_parts = L.num_parts;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     if (va::launch_warp_partial(pp, D, kv_dtype, ni, s) != cudaSuccess) return VA_ERR_CUDA;
     if (ng > 0) {

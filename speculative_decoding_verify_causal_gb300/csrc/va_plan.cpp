@@ -485,6 +485,7 @@ int verify_attn_with_plan(const va_plan *p, const void *q, const void *k_pages,
     pp.R = pp.G * p->T;
     pp.rows_per_group = p->rows_per_group;
     pp.num_pages = p->num_pages;
+    pp.num_parts = p->num_parts;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->D));
 
     if (p->path == VA_PATH_MMA) {
