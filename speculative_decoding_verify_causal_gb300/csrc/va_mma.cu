@@ -215,8 +215,17 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     if (warp == C::kProducerWarp) {
         // Set-up by the producer warp, which then arrives at the set-up
         // barrier without waiting for the others: its first copies go out
-        // while the other warps load Q and allocate TMEM.
+        // while the other warps load Q and allocate TMEM.  The first page
+        // ids are requested before anything else.
+        int pg_first[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = 32 * j + lane;
+            pg_first[j] = k < npages_item ? __ldg(bt + lp0 + k) : 0;
+        }
         if (lane == 0) {
+            prefetch_tensormap(&mp.tm_k);
+            prefetch_tensormap(&mp.tm_v);
             for (int i = 0; i < kMaxRawStages; ++i) {
                 mbar_init(bar(kRawFull + i), 1);
                 mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps : 1);
@@ -229,7 +238,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(bar(kSFull + i), 1);                    // QK^T committed
-                    mbar_init(bar(kPFull + i), C::kSoftmaxWarps);     // softmax has written P
+                mbar_init(bar(kPFull + i), C::kSoftmaxWarps);     // softmax has written P
                 mbar_init(bar(kPEmpty + i), 1);                   // P x V done: S/P buffer free
             }
             mbar_init(bar(kODone), 1);
@@ -237,9 +246,6 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             mbar_init(bar(kQReady), C::kSoftmaxWarps + C::kDequantWarps);
             for (int i = 0; i < kScaleRing; ++i) mbar_init(bar(kRingFree + i), C::kSoftmaxWarps);
             fence_barrier_init();
-            if (p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);
-            prefetch_tensormap(&mp.tm_k);
-            prefetch_tensormap(&mp.tm_v);
         }
         // the item's page ids -> smem (bad entries replaced by page 0 and
         // flagged); four loads per lane in flight at a time
@@ -248,7 +254,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int k = k0 + 32 * j + lane;
-                pg[j] = k < npages_item ? __ldg(bt + lp0 + k) : 0;
+                pg[j] = k0 == 0 ? pg_first[j] : (k < npages_item ? __ldg(bt + lp0 + k) : 0);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -480,6 +486,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             }
             if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
             mma_commit(bar(kOFinal));
+            if (p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);  // off the critical path
             if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         }
     } else if (warp < C::kSoftmaxWarps) {
