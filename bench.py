@@ -132,23 +132,27 @@ def dist_setup(args):
     return world, rank, local
 
 
-def cpu_baseline(w, wl, max_rows=None):
-    """Time the oracle as it stands on the host cores over a bounded sample:
-    the packed rows of kv head 0 of sequence 0 (or the first max_rows of them)."""
+def cpu_baseline(w, wl, min_seconds=10.0):
+    """Time the oracle as it stands on the host cores over a bounded sample of
+    the same workload: chunks of query rows, cycling over all (seq, token,
+    q-head) rows, until at least min_seconds of CPU work have been done."""
     import oracle
-    G = w["Hq"] // w["Hkv"]
-    rows = [(0, t, h) for t in range(w["T"]) for h in range(G)]
-    if max_rows:
-        rows = rows[:max_rows]
+    B, T, Hq = w["q"].shape[:3]
+    all_rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
+    chunk = Hq // w["Hkv"] * T  # the packed rows of one kv head
     cores = oracle.max_threads(0)
-    t0 = time.perf_counter()
-    oracle.verify_attn_rows(w, rows, nthreads=0)
-    dt = time.perf_counter() - t0
-    frac = len(rows) / (w["q"].shape[0] * w["T"] * w["Hq"])
-    byts = wl.algorithmic_bytes(w) * frac
+    n = 0
+    dt = 0.0
+    while dt < min_seconds:
+        rows = [all_rows[(n + k) % len(all_rows)] for k in range(chunk)]
+        t0 = time.perf_counter()
+        oracle.verify_attn_rows(w, rows, nthreads=0)
+        dt += time.perf_counter() - t0
+        n += chunk
+    byts = wl.algorithmic_bytes(w) * n / len(all_rows)
     return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} of {w['q'].shape[0] * w['T'] * w['Hq']} (seq, token, q-head) rows "
-                      f"(kv head 0 of sequence 0), fp64, {dt:.2f} s",
+            "sample": f"{n} query rows ({n / len(all_rows):.2f} x the workload's {len(all_rows)}), "
+                      f"chunks of {chunk}, fp64, {dt:.1f} s",
             "seconds": dt}
 
 
@@ -392,7 +396,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16" if info["path"] == 2 else "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("bf16" if w["kv_dtype"] == "bf16" else "f16") if info["path"] == 2 else "f32", "data": "synthetic",
         "us_per_call": ms_per_step * 1e3,
         "frac_of_peak_hbm": value / world / peak,
         "config": {
