@@ -31,6 +31,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     __shared__ float red[kSlices][D];
     __shared__ float wsm[kSlices * kBatch];
     __shared__ float wred[kSlices];
+    // programmatic dependent launch: the partials are the previous kernel's
+    // output.  (No early trigger here: the next call's partial kernel would
+    // take the SMs this grid still needs.)
+    griddep_wait();
     const Group g = p.groups[blockIdx.x];
     const int r = blockIdx.y;
     const int rr = g.rg * p.rows_per_group + r;
@@ -126,8 +130,7 @@ template <int D>
 cudaError_t launch_d(const CombineParams &p, int num_groups, int max_splits, cudaStream_t s) {
     (void)max_splits;
     dim3 grid(num_groups, p.rows_per_group);
-    combine_kernel<D><<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<D>, grid, dim3(kThreads), 0, s, p);
 }
 
 }  // namespace

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 #include "verify_attn.h"
@@ -52,6 +54,29 @@ struct CombineParams {
     float *lse;
     int T, Hq, G, R, rows_per_group, D;
 };
+
+// Launch `kernel` with programmatic dependent launch allowed: it may start
+// while the previous kernel on the stream is finishing, and must execute
+// griddepcontrol.wait before it touches memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Programmatic dependent launch, device side: wait until the previous grid on
+// the stream has completed and its writes are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Remember a failing CUDA call for verify_attn_last_cuda_error (thread-local).
 void note_cuda_error(cudaError_t e);

@@ -202,6 +202,11 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bars + kNumBars * 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Programmatic dependent launch: the launch may overlap the previous
+    // kernel's tail; wait for it (it may have written the inputs or the work
+    // list) before any load.  No early trigger for the next kernel: the
+    // combine would only take SMs from this grid's tail (measured slower).
+    griddep_wait();
     const Item it = p.items[blockIdx.x];
     const int G = p.G, T = p.T, Hkv = p.Hkv;
     const int row0 = it.rg * p.rows_per_group;
@@ -926,8 +931,7 @@ cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
     auto k = mma_partial_kernel<D, DT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<n, Cfg<D, DT>::kThreads, smem, s>>>(mp);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(n), dim3(Cfg<D, DT>::kThreads), smem, s, mp);
 }
 
 template <int D>

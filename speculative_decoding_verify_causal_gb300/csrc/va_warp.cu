@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreads) warp_partial_kernel(const PartialPar
     constexpr int EPC = 16 / EB;                    // elements per 16-byte chunk
     constexpr int CPR = D / EPC;                    // chunks per cache row
     constexpr int DPT = (D + kThreads - 1) / kThreads;  // head_dim slice per thread
+    // programmatic dependent launch: nothing of the caller's is touched before this
+    griddep_wait();
 
     extern __shared__ float smem[];
     float *Qs = smem;                 // [RB][D]   q * log2(e)/sqrt(D)
@@ -287,8 +289,7 @@ cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
     auto k = warp_partial_kernel<D, DT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<n, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(n), dim3(kThreads), smem, s, p);
 }
 
 template <int D>
