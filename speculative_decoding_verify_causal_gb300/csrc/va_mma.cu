@@ -657,35 +657,46 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             if (lane == 0) mbar_arrive(bar(kPFull + b));
         }
         // epilogue: O / l and the log-sum-exp (the pair adds its partial sums).
-        // Each row's normalised output is staged in the tile buffers (free once
-        // the last P x V has completed), 16-byte units XOR-swizzled by row so
-        // that neither the row-per-thread writes nor the reads conflict, then
-        // all softmax threads copy the item's rows out with consecutive
-        // 16-byte stores: fp32 into the split partials, or bf16 into out for
-        // an unsplit item.
+        // An unsplit item's rows go to out as bf16: staged in the tile buffers
+        // (free once the last P x V has completed), 16-byte units XOR-swizzled
+        // by row, then copied out with consecutive 16-byte stores.  A split's
+        // fp32 partials are staged as the boxes of the partials' tensor map
+        // and leave by TMA, one 32-column chunk at a time, each store starting
+        // as soon as the four warps of its half have staged it.
         if (!mbar_wait(bar(kOFinal), 0, kWaitNs)) ok = false;
         tc_fence_after();
         const bool final_out = it.part < 0;
         const int cb = D / 8;  // 16-byte units per staged bf16 row
         const uint32_t stage = sbase + L.conv_k;
-        // fp32 partials: 32-column (128-byte) chunks, each the box of the
-        // partials' tensor map (rows padded to 8 keep every box 1024-byte aligned)
+        // fp32 chunk stride (rows padded to 8 keep every box 1024-byte aligned)
         const uint32_t cstride = (uint32_t)((p.rows_per_group + 7) / 8 * 8) * 128u;
         auto unit = [](int row, int c) { return (uint32_t)(((c & ~7) | ((c ^ row) & 7)) << 4); };
+        float inv = 0.f;
         if (warp_active) {
             sts_f32(xsum + 4u * (half * 128 + r), l_run);
             named_bar_sync(pair_bar, 64);
             const float l_tot = l_run + lds_f32(xsum + 4u * ((1 - half) * 128 + r));
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const float lse_nat = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
-            const uint32_t srow = stage + (uint32_t)(r * cb * 16);
-#pragma unroll 1
-            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_tm + C::kOCol + c0, o);
-                tmem_wait_ld();
-                if (!row_ok) continue;
+            if (row_ok && half == 0 && ok) {  // the row's log-sum-exp
+                const int rr = row0 + r;
+                const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + it.kvh * G + rr % G;
                 if (final_out) {
+                    if (p.lse) p.lse[orow] = lse_nat;
+                } else {
+                    p.lse_part[(size_t)it.part * p.rows_per_group + r] = lse_nat;
+                }
+            }
+        }
+        if (final_out) {
+            if (warp_active) {
+                const uint32_t srow = stage + (uint32_t)(r * cb * 16);
+#pragma unroll 1
+                for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_tm + C::kOCol + c0, o);
+                    tmem_wait_ld();
+                    if (!row_ok) continue;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint4 w;
@@ -695,50 +706,50 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         w.w = pack_bf162(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
                         sts_u4(srow + unit(r, c0 / 8 + k), w);
                     }
-                } else {
-                    // row r of chunk c0 / 32, 16-byte units XOR-swizzled by r % 8
-                    // (the tensor map's 128-byte swizzle; also conflict-free here)
-                    const uint32_t crow = stage + (uint32_t)(c0 / 32) * cstride + (uint32_t)r * 128u;
+                }
+            }
+            named_bar_sync(9, C::kSoftmaxWarps * 32);  // all rows staged
+            if (ok) {
+                const int st = warp * 32 + lane;  // 0 .. 255
+                for (int e = st; e < nrows * cb; e += C::kSoftmaxWarps * 32) {
+                    const int row = e / cb, c = e % cb;
+                    const uint4 v = lds_u4(stage + (uint32_t)(row * cb * 16) + unit(row, c));
+                    const int rr = row0 + row;
+                    const size_t orow = (size_t)(it.b * T + rr / G) * p.Hq + it.kvh * G + rr % G;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.out) + orow * D * 2 + c * 16) = v;
+                }
+            }
+        } else {
+            // rows past nrows in a box are padding that nothing reads
+            const bool issuer = ok && quarter == 0 && lane == 0;
+#pragma unroll 1
+            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+                const uint32_t chunk = stage + (uint32_t)(c0 / 32) * cstride;
+                if (warp_active) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_tm + C::kOCol + c0, o);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        // row r of the chunk, 16-byte units XOR-swizzled by r % 8 (the
+                        // tensor map's 128-byte swizzle; also conflict-free here)
+                        const uint32_t crow = chunk + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        sts_u4(crow + ((k ^ (r & 7)) << 4),
-                               make_uint4(__float_as_uint(__uint_as_float(o[4 * k]) * inv),
-                                          __float_as_uint(__uint_as_float(o[4 * k + 1]) * inv),
-                                          __float_as_uint(__uint_as_float(o[4 * k + 2]) * inv),
-                                          __float_as_uint(__uint_as_float(o[4 * k + 3]) * inv)));
-                }
-            }
-            if (!final_out) fence_proxy_async_smem();  // staged rows -> the TMA store
-            if (row_ok && half == 0) {
-                // the row's log-sum-exp
-                if (ok) {
-                    const int rr = row0 + r;
-                    const size_t orow = (size_t)(it.b * T + t_r) * p.Hq + it.kvh * G + rr % G;
-                    if (final_out) {
-                        if (p.lse) p.lse[orow] = lse_nat;
-                    } else {
-                        p.lse_part[(size_t)it.part * p.rows_per_group + r] = lse_nat;
+                        for (int k = 0; k < 8; ++k)
+                            sts_u4(crow + ((k ^ (r & 7)) << 4),
+                                   make_uint4(__float_as_uint(__uint_as_float(o[4 * k]) * inv),
+                                              __float_as_uint(__uint_as_float(o[4 * k + 1]) * inv),
+                                              __float_as_uint(__uint_as_float(o[4 * k + 2]) * inv),
+                                              __float_as_uint(__uint_as_float(o[4 * k + 3]) * inv)));
                     }
+                    fence_proxy_async_smem();  // staged rows -> the TMA store
+                }
+                named_bar_sync(11 + half, 128);  // the half's four warps have staged this chunk
+                if (issuer) {
+                    tma_store_2d(&mp.tm_o, c0, it.part * p.rows_per_group, chunk);
+                    bulk_commit_group();
                 }
             }
-        }
-        named_bar_sync(9, C::kSoftmaxWarps * 32);  // all rows staged
-        if (ok && final_out) {
-            const int st = warp * 32 + lane;  // 0 .. 255
-            for (int e = st; e < nrows * cb; e += C::kSoftmaxWarps * 32) {
-                const int row = e / cb, c = e % cb;
-                const uint4 v = lds_u4(stage + (uint32_t)(row * cb * 16) + unit(row, c));
-                const int rr = row0 + row;
-                const size_t orow = (size_t)(it.b * T + rr / G) * p.Hq + it.kvh * G + rr % G;
-                *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(p.out) + orow * D * 2 + c * 16) = v;
-            }
-        } else if (ok && warp == 0 && lane == 0) {
-            // the item's block of partials (rows past nrows are padding that
-            // nothing reads) leaves in D / 32 box stores
-            for (int k = 0; k < D / 32; ++k)
-                tma_store_2d(&mp.tm_o, k * 32, it.part * p.rows_per_group, stage + (uint32_t)k * cstride);
-            bulk_commit_group();
-            bulk_wait_group_read0();  // shared memory stays valid until the stores have read it
+            if (issuer) bulk_wait_group_read0();  // shared memory stays valid until the stores have read it
         }
     } else if constexpr (C::kQuant) {
         // ------------------------------------------------------------ dequant
