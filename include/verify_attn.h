@@ -232,6 +232,42 @@ int verify_attn_noalloc(const int32_t *seq_lens_host, int num_seqs, int T,
                         const int32_t *seq_lens, void *out, float *lse,
                         void *stream);
 
+/* KV append with quantise-on-write: the step just before verify attention.
+ * The verify forward computes K and V for its T tokens and stores them in the
+ * paged cache before attending ("I pushed Qwen3.8-27B to 381 tps for a single
+ * request on a RTX 3090", "DFlash2 past 64k": an int8 cache in 16-token
+ * pages; "I pushed Qwen3.8-27B to 124 tps on a single request on a RTX
+ * 3090", "What we had": an fp8 cache).  For sequence b (L_b = seq_lens[b]
+ * includes the T new tokens), verify token t and kv head g:
+ *     pos  = L_b - T + t,  page = block_table[b][pos / 16],  slot = pos % 16
+ *     x    = k_new[b, t, g, :]                (bf16, exact in fp32)
+ *     a    = max_d |x_d|
+ *     s    = a / qmax in fp32, qmax = 448 (e4m3) or 127 (int8); s = 1 if a = 0
+ *     y_d  = x_d / s in fp32 (correctly rounded)
+ *     e4m3: byte_d = round-to-nearest-even e4m3 of clamp(y_d, -448, 448)
+ *     int8: byte_d = clamp(round-half-even(y_d), -127, 127)
+ *     k_pages[page, slot, g, :] = byte,  k_scale[page, slot, g] = s
+ * and the same for v.  A bf16 cache receives the bf16 bits unchanged (the
+ * scale pointers are ignored and may be NULL).  This is the per-(token, kv
+ * head) absmax quantisation the verify inputs are built with, so appending
+ * and attending agree on the cache format.
+ *
+ * Layouts: k_new, v_new bf16 [num_seqs, T, Hkv, D] on the device; the cache,
+ * block table (row stride block_table_stride >= 1) and device seq_lens as for
+ * verify_attn.  head_dim in {64, 128, 256}.  Checks: rows whose position is
+ * negative (seq_lens[b] < T) or whose page is outside [0, num_pages) (when
+ * num_pages > 0) are skipped and set bit 0 of *flags (a device int, may be
+ * NULL; the library only ORs into it).  Returns VA_OK when enqueued on
+ * stream, VA_ERR_INVALID_ARGUMENT for null or non-positive arguments,
+ * VA_ERR_UNSUPPORTED for another head_dim or dtype, VA_ERR_CUDA if the launch
+ * fails.  Rows of one call write disjoint cache slots as long as the block
+ * table does not map two of them to the same page and slot. */
+int verify_attn_kv_append(const void *k_new, const void *v_new, int num_seqs, int T,
+                          int num_kv_heads, int head_dim, va_kv_dtype kv_dtype,
+                          void *k_pages, void *v_pages, float *k_scale, float *v_scale,
+                          const int32_t *block_table, int block_table_stride,
+                          const int32_t *seq_lens, int num_pages, int *flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

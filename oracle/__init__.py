@@ -3,8 +3,9 @@
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` import this package.  The C source ``verify_attn_oracle.c`` is the
 plain fp64 definition of the verify step's causal GQA attention over a paged,
-quantised KV cache; this module compiles it with gcc and marshals numpy arrays
-into it.  It shares no code with the CUDA library.
+quantised KV cache, and ``kv_append_oracle.c`` the definition of the KV append
+with quantise-on-write that precedes it; this module compiles them with gcc and
+marshals numpy arrays into them.  It shares no code with the CUDA library.
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "verify_attn_oracle.c")
+_SRCS = [os.path.join(_HERE, "verify_attn_oracle.c"), os.path.join(_HERE, "kv_append_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -26,10 +27,12 @@ KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "int8": 2}
 
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/liboracle.so`` (gcc, OpenMP)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    # -ffp-contract=off: the append oracle's binary32 arithmetic must not be fused
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -56,6 +59,12 @@ def _load():
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_max_threads.argtypes = [I]
         lib.oracle_max_threads.restype = I
+        lib.oracle_kv_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, I, P, I, P]
+        lib.oracle_kv_append.restype = I
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_int8_encode.argtypes = [ctypes.c_float]
+        lib.oracle_int8_encode.restype = ctypes.c_int8
         _lib = lib
         return lib
 
@@ -138,3 +147,35 @@ def decode_bf16(bits: int) -> float:
 
 def max_threads(nthreads: int = 0) -> int:
     return _load().oracle_max_threads(nthreads)
+
+
+def e4m3_encode(y: float) -> int:
+    """Round-to-nearest-even e4m3 code of a binary32 value (|y| <= 448)."""
+    return int(_load().oracle_e4m3_encode(float(y)))
+
+
+def int8_encode(y: float) -> int:
+    return int(_load().oracle_int8_encode(float(y)))
+
+
+def kv_append(k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, kv_dtype,
+              num_pages: int = 0):
+    """Append new K/V rows (bf16 bits, [B, T, Hkv, D]) into copies of the given
+    cache arrays; returns (k_pages, v_pages, k_scale, v_scale, skipped)."""
+    lib = _load()
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    B, T, Hkv, D = k_new.shape
+    kp = np.array(k_pages, copy=True, order="C")
+    vp = np.array(v_pages, copy=True, order="C")
+    ks = None if k_scale is None else np.array(k_scale, dtype=np.float32, copy=True, order="C")
+    vs = None if v_scale is None else np.array(v_scale, dtype=np.float32, copy=True, order="C")
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    skipped = ctypes.c_int(0)
+    rc = lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), B, T, Hkv, D, KV_DTYPES[kv_dtype], _ptr(kp), _ptr(vp),
+                              _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1], _ptr(sl), int(num_pages),
+                              ctypes.byref(skipped))
+    if rc != 0:
+        raise ValueError("oracle_kv_append rejected its arguments")
+    return kp, vp, ks, vs, skipped.value

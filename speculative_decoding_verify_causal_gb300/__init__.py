@@ -98,6 +98,8 @@ def _load():
         lib.verify_attn_last_cuda_error_string.restype = ctypes.c_char_p
         lib.verify_attn_noalloc.argtypes = [P, I, I, I, I, I, I] + [P] * 6 + [I, P, P, P, P]
         lib.verify_attn_noalloc.restype = I
+        lib.verify_attn_kv_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, I, P, I, P, P]
+        lib.verify_attn_kv_append.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
                   "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
             getattr(lib, f).restype = I
@@ -322,7 +324,37 @@ def verify_attn_noalloc(seq_lens_host, T, num_q_heads, num_kv_heads, head_dim, k
     _check(rc, "verify_attn_noalloc")
 
 
+def verify_attn_kv_append(k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, T,
+                          kv_dtype, num_pages=0, flags=None, stream=None):
+    """KV append with quantise-on-write: store the T new tokens' K and V rows
+    (bf16 ``[B, T, Hkv, D]``) at positions ``seq_lens[b] - T + t`` of the paged
+    cache, quantised per (token, kv head) for fp8 / int8 caches (definition in
+    ``include/verify_attn.h``).  ``flags`` is an optional int32 device tensor
+    into which bit 0 is ORed for a skipped row."""
+    import torch
+    code = _dtype_code(kv_dtype)
+    B, T_, Hkv, D = k_new.shape
+    if int(T) != T_ or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new and v_new must both be [B, T, Hkv, D] with the given T")
+    q16 = (torch.bfloat16, torch.int16)
+    kvd = _kv_dtypes(code)
+    ptrs = [_dev_ptr(k_new, "k_new", q16), _dev_ptr(v_new, "v_new", q16)]
+    cache = [_dev_ptr(k_pages, "k_pages", kvd), _dev_ptr(v_pages, "v_pages", kvd),
+             _dev_ptr(k_scale, "k_scale", (torch.float32,), allow_none=code == VA_BF16),
+             _dev_ptr(v_scale, "v_scale", (torch.float32,), allow_none=code == VA_BF16)]
+    bt = _dev_ptr(block_table, "block_table", (torch.int32,))
+    sl = _dev_ptr(seq_lens, "seq_lens", (torch.int32,))
+    fl = _dev_ptr(flags, "flags", (torch.int32,), allow_none=True)
+    if stream is None:
+        stream = torch.cuda.current_stream(k_new.device)
+    st = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    rc = _load().verify_attn_kv_append(*ptrs, int(B), int(T), int(Hkv), int(D), code, *cache, bt,
+                                       int(block_table.shape[1]), sl, int(num_pages), fl, st)
+    _check(rc, "verify_attn_kv_append")
+
+
 __all__ = [
+    "verify_attn_kv_append",
     "verify_attn_noalloc",
     "verify_attn_plan_set_events",
     "verify_attn_plan", "verify_attn", "verify_attn_with_plan", "verify_attn_plan_destroy",
