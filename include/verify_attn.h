@@ -268,6 +268,33 @@ int verify_attn_kv_append(const void *k_new, const void *v_new, int num_seqs, in
                           const int32_t *block_table, int block_table_stride,
                           const int32_t *seq_lens, int num_pages, int *flags, void *stream);
 
+/* Lookup-augmented drafting: propose draft tokens by finding the most recent
+ * earlier occurrence of the request's last generated tokens in its own token
+ * history and copying what followed ("I pushed Qwen3.8-27B to 381 tps for a
+ * single request on a RTX 3090", "Lookup-augmented drafting": the last 6-12
+ * tokens are looked up in the whole history, far beyond a block drafter's
+ * window).  For sequence b with history x[0 .. L-1] (L = lens[b]):
+ *     l(e)  = the largest l <= max_match with x[e - i] == x[L - 1 - i] for all
+ *             i < l (and e - i >= 0), for every end position e <= L - 2
+ *             (so that at least one token follows the occurrence);
+ *     best  = the e with the largest min(l(e), max_match) among those with
+ *             l(e) >= min_match, the largest e (the most recent) on a tie;
+ *     draft = x[e + 1 .. min(e + 1 + num_draft, L) - 1]
+ * draft_len[b] = its length (0 when no e qualifies), draft slots past it are
+ * -1, match_end[b] = e or -1 (may be NULL), match_len[b] = min(l(e),
+ * max_match) or 0 (may be NULL).  Integer work: the result is exact.
+ *
+ * Layouts (device): tokens int32 [num_seqs, token_stride]; lens int32
+ * [num_seqs] (0 <= lens[b] <= token_stride); draft int32 [num_seqs,
+ * num_draft]; draft_len, match_end, match_len int32 [num_seqs].  Limits:
+ * 1 <= min_match <= max_match <= 32, 1 <= num_draft <= 256.  Returns VA_OK
+ * when enqueued, VA_ERR_INVALID_ARGUMENT otherwise, VA_ERR_CUDA if the launch
+ * fails.  One CTA scans each sequence. */
+int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int32_t *lens,
+                             int num_seqs, int min_match, int max_match, int num_draft,
+                             int32_t *draft, int32_t *draft_len, int32_t *match_end,
+                             int32_t *match_len, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

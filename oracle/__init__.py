@@ -3,8 +3,9 @@
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` import this package.  The C source ``verify_attn_oracle.c`` is the
 plain fp64 definition of the verify step's causal GQA attention over a paged,
-quantised KV cache, and ``kv_append_oracle.c`` the definition of the KV append
-with quantise-on-write that precedes it; this module compiles them with gcc and
+quantised KV cache, ``kv_append_oracle.c`` the definition of the KV append
+with quantise-on-write that precedes it and ``lookup_draft_oracle.c`` the
+lookup-augmented drafter's history scan; this module compiles them with gcc and
 marshals numpy arrays into them.  It shares no code with the CUDA library.
 """
 from __future__ import annotations
@@ -17,7 +18,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "verify_attn_oracle.c"), os.path.join(_HERE, "kv_append_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("verify_attn_oracle.c", "kv_append_oracle.c", "lookup_draft_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +66,8 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_int8_encode.argtypes = [ctypes.c_float]
         lib.oracle_int8_encode.restype = ctypes.c_int8
+        lib.oracle_lookup_draft.argtypes = [P, I, I, I, I, P, P, P]
+        lib.oracle_lookup_draft.restype = I
         _lib = lib
         return lib
 
@@ -179,3 +182,16 @@ def kv_append(k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq
     if rc != 0:
         raise ValueError("oracle_kv_append rejected its arguments")
     return kp, vp, ks, vs, skipped.value
+
+
+def lookup_draft(history, min_match: int, max_match: int, num_draft: int):
+    """Lookup-augmented draft of one token history (int32 [L]): returns
+    (draft [num_draft] with -1 past the proposal, draft_len, match_end, match_len)."""
+    lib = _load()
+    x = _c(history, np.int32)
+    draft = np.empty(num_draft, np.int32)
+    e = ctypes.c_int32(0)
+    n = ctypes.c_int32(0)
+    length = lib.oracle_lookup_draft(_ptr(x), int(x.size), int(min_match), int(max_match), int(num_draft),
+                                     _ptr(draft), ctypes.byref(e), ctypes.byref(n))
+    return draft, int(length), int(e.value), int(n.value)

@@ -100,6 +100,8 @@ def _load():
         lib.verify_attn_noalloc.restype = I
         lib.verify_attn_kv_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, I, P, I, P, P]
         lib.verify_attn_kv_append.restype = I
+        lib.verify_attn_lookup_draft.argtypes = [P, I, P, I, I, I, I, P, P, P, P, P]
+        lib.verify_attn_lookup_draft.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
                   "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
             getattr(lib, f).restype = I
@@ -353,7 +355,38 @@ def verify_attn_kv_append(k_new, v_new, k_pages, v_pages, k_scale, v_scale, bloc
     _check(rc, "verify_attn_kv_append")
 
 
+def verify_attn_lookup_draft(tokens, lens, num_draft, min_match=6, max_match=12, match_end=None,
+                            match_len=None, stream=None):
+    """Lookup-augmented drafting over token histories ``tokens`` (int32 CUDA
+    tensor ``[num_seqs, stride]``, the first ``lens[b]`` entries valid): the
+    most recent earlier occurrence of each history's last tokens (longest
+    match first, ``min_match``..``max_match``) and up to ``num_draft`` tokens
+    that followed it.  Returns (draft int32 ``[num_seqs, num_draft]``, -1 past
+    the proposal, draft_len int32 ``[num_seqs]``); ``match_end`` /
+    ``match_len`` (int32 ``[num_seqs]``) are filled when given."""
+    import torch
+    if tokens.dim() != 2:
+        raise ValueError("tokens must be [num_seqs, stride]")
+    B, stride = tokens.shape
+    i32 = (torch.int32,)
+    tp = _dev_ptr(tokens, "tokens", i32)
+    lp = _dev_ptr(lens, "lens", i32)
+    draft = torch.empty((B, int(num_draft)), dtype=torch.int32, device=tokens.device)
+    dlen = torch.empty((B,), dtype=torch.int32, device=tokens.device)
+    me = _dev_ptr(match_end, "match_end", i32, allow_none=True)
+    ml = _dev_ptr(match_len, "match_len", i32, allow_none=True)
+    if stream is None:
+        stream = torch.cuda.current_stream(tokens.device)
+    st = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    rc = _load().verify_attn_lookup_draft(tp, int(stride), lp, int(B), int(min_match), int(max_match),
+                                          int(num_draft), ctypes.c_void_p(draft.data_ptr()),
+                                          ctypes.c_void_p(dlen.data_ptr()), me, ml, st)
+    _check(rc, "verify_attn_lookup_draft")
+    return draft, dlen
+
+
 __all__ = [
+    "verify_attn_lookup_draft",
     "verify_attn_kv_append",
     "verify_attn_noalloc",
     "verify_attn_plan_set_events",

@@ -262,3 +262,24 @@ def to_device(w, device="cuda", copies=1):
         "out": torch.zeros((B, T, Hq, D), dtype=torch.bfloat16, device=dev),
         "lse": torch.zeros((B, T, Hq), dtype=torch.float32, device=dev),
     }
+
+
+def token_history(seed: int, length: int, vocab: int = 151_936, copy_frac: float = 0.3,
+                  seg_range=(8, 64)) -> np.ndarray:
+    """Synthetic token stream for lookup-augmented drafting: uniform tokens in
+    [0, vocab), with about ``copy_frac`` of the stream made of segments copied
+    verbatim from earlier in the stream (a long-context assistant quoting what
+    it was given), lengths uniform in ``seg_range``.  int32 [length]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.integers(0, vocab, length, dtype=np.int64).astype(np.int32)
+    pos = seg_range[1] * 2
+    while pos < length:
+        if rng.random() < copy_frac:
+            n = int(rng.integers(seg_range[0], seg_range[1] + 1))
+            n = min(n, length - pos)
+            src = int(rng.integers(0, pos - n)) if pos - n > 0 else 0
+            x[pos:pos + n] = x[src:src + n]
+            pos += n
+        else:
+            pos += int(rng.integers(seg_range[0], seg_range[1] + 1))
+    return x
