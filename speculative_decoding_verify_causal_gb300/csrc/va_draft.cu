@@ -2,13 +2,17 @@
 // request on a RTX 3090", "Lookup-augmented drafting"): find the most recent
 // earlier occurrence of the history's last tokens and propose what followed.
 //
-// One CTA per sequence.  The last max_match tokens (reversed) sit in shared
-// memory; every thread walks end positions e = tid, tid + blockDim, ...
-// (coalesced 4-byte loads of x[e]), extends a match backwards only when x[e]
-// equals the last token, and keeps the best (length, e) as one 64-bit key
-// (length in the high word, so the maximum is the longest match and, among
-// equal lengths, the most recent end).  A block max-reduction picks the
-// winner and the first num_draft threads copy the continuation.
+// One thread-block cluster per sequence (1 to 8 CTAs, from the history
+// length bound): CTA r scans the r-th slice of the end positions.  The last
+// max_match tokens (reversed) sit in each CTA's shared memory; every thread
+// walks end positions e (coalesced 4-byte loads of x[e]), extends a match
+// backwards only when x[e] equals the last token, and keeps the best
+// (length, e) as one 64-bit key (length in the high word, so the maximum is
+// the longest match and, among equal lengths, the most recent end).  A block
+// max-reduction, then CTA 0 reads the other CTAs' keys through distributed
+// shared memory and its first num_draft threads copy the continuation.
+#include <algorithm>
+
 #include "va_internal.h"
 
 namespace va {
@@ -16,6 +20,8 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kMaxMatch = 32;
+constexpr int kMaxCluster = 8;          // portable cluster size
+constexpr int kTokensPerCta = 16384;    // history slice one CTA scans, at most (sets the cluster size)
 
 struct DraftParams {
     const int32_t *tokens;
@@ -23,6 +29,33 @@ struct DraftParams {
     int32_t *draft, *draft_len, *match_end, *match_len;
     int stride, min_match, max_match, num_draft;
 };
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 64-bit load from the shared memory of CTA `rank` of this cluster, at the
+// address `local` has in this CTA.
+__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, uint32_t rank) {
+    uint32_t remote;
+    const uint32_t addr = (uint32_t)__cvta_generic_to_shared(local);
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll
@@ -37,7 +70,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const DraftParams p) {
     __shared__ int32_t suf[kMaxMatch];                  // suf[i] = x[L - 1 - i]
     __shared__ unsigned long long wbest[kThreads / 32];
     griddep_wait();  // the history may come from the previous kernel on the stream
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = (int)cluster_rank(), nct = (int)cluster_size();
     const int32_t *x = p.tokens + (size_t)b * p.stride;
     int L = p.lens[b];
     if (L < 0 || L > p.stride) L = 0;  // out-of-contract length: treated as an empty history
@@ -47,7 +81,10 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const DraftParams p) {
     unsigned long long best = 0;
     if (lmax >= p.min_match) {
         const int32_t last = suf[0];
-        for (int e = tid; e <= L - 2; e += kThreads) {
+        // this CTA's slice of end positions [0, L - 2]
+        const int n_end = max(L - 1, 0), per = (n_end + nct - 1) / nct;
+        const int e_hi = min(n_end, (rank + 1) * per);
+        for (int e = rank * per + tid; e < e_hi; e += kThreads) {
             if (x[e] != last) continue;
             int l = 1;
             while (l < lmax && e - l >= 0 && x[e - l] == suf[l]) ++l;
@@ -64,17 +101,24 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const DraftParams p) {
         best = warp_max_u64(lane < kThreads / 32 ? wbest[lane] : 0ull);
         if (lane == 0) wbest[0] = best;
     }
-    __syncthreads();
-    best = wbest[0];
-    const int e = best ? (int)(best & 0xffffffffull) : -1;
-    const int n = best ? min(p.num_draft, L - 1 - e) : 0;
-    for (int t = tid; t < p.num_draft; t += kThreads)
-        p.draft[(size_t)b * p.num_draft + t] = t < n ? x[e + 1 + t] : -1;
-    if (tid == 0) {
-        p.draft_len[b] = n;
-        if (p.match_end) p.match_end[b] = e;
-        if (p.match_len) p.match_len[b] = best ? (int)(best >> 32) : 0;
+    cluster_sync();  // every CTA's key is in its shared memory
+    if (rank == 0) {
+        best = wbest[0];
+        for (int r = 1; r < nct; ++r) {
+            const unsigned long long o = ld_cluster_u64(&wbest[0], (uint32_t)r);
+            best = o > best ? o : best;
+        }
+        const int e = best ? (int)(best & 0xffffffffull) : -1;
+        const int n = best ? min(p.num_draft, L - 1 - e) : 0;
+        for (int t = tid; t < p.num_draft; t += kThreads)
+            p.draft[(size_t)b * p.num_draft + t] = t < n ? x[e + 1 + t] : -1;
+        if (tid == 0) {
+            p.draft_len[b] = n;
+            if (p.match_end) p.match_end[b] = e;
+            if (p.match_len) p.match_len[b] = best ? (int)(best >> 32) : 0;
+        }
     }
+    cluster_sync();  // the other CTAs' shared memory stays valid until CTA 0 has read it
 }
 
 }  // namespace
@@ -85,7 +129,7 @@ extern "C" int verify_attn_lookup_draft(const int32_t *tokens, int token_stride,
                                         int32_t *draft, int32_t *draft_len, int32_t *match_end,
                                         int32_t *match_len, void *stream) {
     if (!tokens || !lens || !draft || !draft_len) return VA_ERR_INVALID_ARGUMENT;
-    if (num_seqs < 1 || token_stride < 1 || min_match < 1 || max_match < min_match ||
+    if (num_seqs < 1 || num_seqs > 65535 || token_stride < 1 || min_match < 1 || max_match < min_match ||
         max_match > va::kMaxMatch || num_draft < 1 || num_draft > 256)
         return VA_ERR_INVALID_ARGUMENT;
     va::DraftParams p{};
@@ -99,8 +143,22 @@ extern "C" int verify_attn_lookup_draft(const int32_t *tokens, int token_stride,
     p.min_match = min_match;
     p.max_match = max_match;
     p.num_draft = num_draft;
-    const cudaError_t e = va::launch_pdl(va::lookup_kernel, dim3(num_seqs), dim3(va::kThreads), 0,
-                                         static_cast<cudaStream_t>(stream), p);
+    // cluster of CTAs per sequence: one per kTokensPerCta of the longest possible history
+    const int nct = std::min(va::kMaxCluster, std::max(1, (token_stride + va::kTokensPerCta - 1) / va::kTokensPerCta));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nct, num_seqs);
+    cfg.blockDim = dim3(va::kThreads);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nct;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, va::lookup_kernel, p);
     if (e != cudaSuccess) {
         va::note_cuda_error(e);
         return VA_ERR_CUDA;
