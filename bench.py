@@ -301,6 +301,44 @@ def lookup_draft_timing(va, wl, w, reps=50):
             "note": "verify_attn_lookup_draft, 6..12-token match, 16 drafts, one CTA per sequence"}
 
 
+def accept_timing(va, w, reps=20, vocab=151_936):
+    """Speculative acceptance for the config's sequences and T drafts over a
+    151,936-token vocabulary (fp32 logits, about 30 % of drafts mismatching),
+    greedy and sampled with point-mass proposals: CUDA events around graphs
+    of `reps` calls."""
+    import torch
+    B, T = len(w["seq_lens"]), w["T"]
+    g = torch.Generator(device="cpu").manual_seed(11)
+    z = torch.randn((B, T + 1, vocab), generator=g).cuda()
+    d = z[:, :T].argmax(-1).to(torch.int32)
+    flip = torch.rand((B, T), generator=g).cuda() < 0.3
+    d = torch.where(flip, torch.randint(0, vocab, (B, T), generator=g).cuda().to(torch.int32), d)
+    res = {"vocab": vocab, "logit_bytes": B * (T + 1) * vocab * 4}
+    for name, t in (("greedy", 0.0), ("sampled", 0.8)):
+        tau = torch.full((B,), t, dtype=torch.float32, device="cuda")
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                va.verify_attn_accept(z, d, tau, 7, stream=stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            s = torch.cuda.current_stream()
+            for i in range(reps):
+                va.verify_attn_accept(z, d, tau, 7 + i, stream=s)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_us_per_call"] = e0.elapsed_time(e1) * 1e3 / reps
+    res["note"] = "verify_attn_accept (stats + decide kernels), logits hot in L2 when they fit"
+    return res
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -479,6 +517,7 @@ def run_ours(args):
 
     append = kv_append_timing(va, w, d, stream)
     lookup = lookup_draft_timing(va, wl, w)
+    acc = accept_timing(va, w)
 
     if rank != 0:
         plan.destroy()
@@ -518,6 +557,7 @@ def run_ours(args):
         "hot_l2": hot,
         "kv_append": append,
         "lookup_draft": lookup,
+        "accept": acc,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,

@@ -62,6 +62,7 @@
 #ifndef VERIFY_ATTN_H
 #define VERIFY_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -294,6 +295,50 @@ int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int3
                              int num_seqs, int min_match, int max_match, int num_draft,
                              int32_t *draft, int32_t *draft_len, int32_t *match_end,
                              int32_t *match_len, void *stream);
+
+/* Speculative acceptance after the verify pass (the rejection sampler).
+ * "I pushed Qwen3.8-27B to 124 tps ...": speculative decoding is exact by
+ * construction (the sampled distribution is the target's); "I pushed
+ * Qwen3.8-27B to 381 tps ...", "Lookup-augmented drafting": greedy never reads
+ * the draft distribution, and sampled positions of a lookup draft get a
+ * point-mass proposal q, which is a legal proposal for the rejection sampler;
+ * "DFlash2 drafting": a model drafter's proposal is softmax of its raw logits
+ * with the temperature applied once.
+ *
+ * For sequence b with draft d[0..T-1], target logits z[t] (t = 0..T, z[T] is
+ * the position after the last draft) and temperature tau = temperature[b]:
+ *   tau <= 0 (greedy): y_t = argmax_i z[t][i] (smallest i on ties); accept
+ *     d[t] while d[t] == y_t; the first mismatch emits y_t, otherwise the
+ *     bonus y_T is emitted.
+ *   tau > 0: p_t = softmax(z[t] / tau); q_t = the one-hot of d[t] when
+ *     draft_logits is NULL, else softmax(draft_logits[t] / tau).  Draft t is
+ *     accepted iff u_t * q_t(d[t]) < p_t(d[t]), u_t = U(b, t, 0, 0).  At the
+ *     first rejection the token emitted is argmax_i [ln r_i + G_i] over
+ *     r_i = max(0, p_t(i) - q_t(i)) > 0 (the residual distribution sampled by
+ *     an exponential race); if every draft is accepted the bonus token is
+ *     argmax_i [z[T][i] / tau + G_i] (a sample of p_T).  G_i = -ln(-ln
+ *     U(b, t, i, 1)) are Gumbel variates of the emitting position t.
+ *   U(b, t, i, k) = (floor(w / 2^8) + 0.5) / 2^24 with w the first word of
+ *     Philox4x32-10 (Salmon et al., SC'11) on counter (i, t, b, k) and key
+ *     (seed low word, seed high word): uniform in (0, 1), reproducible.
+ * Outputs: out_tokens[b, 0 .. n-1] = d[0 .. n-1], out_tokens[b, n] = the
+ * emitted token, -1 after it; num_accepted[b] = n (0 .. T).
+ * Layouts (device): target_logits fp32 [num_seqs, T + 1, vocab];
+ * draft_logits fp32 [num_seqs, T, vocab] or NULL; draft_tokens int32
+ * [num_seqs, T]; temperature fp32 [num_seqs]; out_tokens int32 [num_seqs,
+ * T + 1]; num_accepted int32 [num_seqs]; workspace: at least
+ * verify_attn_accept_workspace_bytes(num_seqs, T) bytes, 16-byte aligned,
+ * owned by the caller.  The decisions are taken in binary32 (the scores,
+ * exponentials and logarithms of the CUDA math library), so a CPU restatement
+ * in another precision agrees except where two scores, or u and p/q, are
+ * within a few ulps.  Returns VA_OK when enqueued, VA_ERR_INVALID_ARGUMENT
+ * for bad arguments (T >= 1, vocab >= 1, draft tokens outside [0, vocab) are
+ * rejected as drafts), VA_ERR_CUDA if a launch fails. */
+size_t verify_attn_accept_workspace_bytes(int num_seqs, int T);
+int verify_attn_accept(const float *target_logits, const float *draft_logits,
+                       const int32_t *draft_tokens, const float *temperature, int num_seqs,
+                       int T, int vocab, uint64_t seed, void *workspace, int32_t *out_tokens,
+                       int32_t *num_accepted, void *stream);
 
 #ifdef __cplusplus
 }

@@ -102,6 +102,10 @@ def _load():
         lib.verify_attn_kv_append.restype = I
         lib.verify_attn_lookup_draft.argtypes = [P, I, P, I, I, I, I, P, P, P, P, P]
         lib.verify_attn_lookup_draft.restype = I
+        lib.verify_attn_accept_workspace_bytes.argtypes = [I, I]
+        lib.verify_attn_accept_workspace_bytes.restype = ctypes.c_size_t
+        lib.verify_attn_accept.argtypes = [P, P, P, P, I, I, I, ctypes.c_uint64, P, P, P, P]
+        lib.verify_attn_accept.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
                   "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
             getattr(lib, f).restype = I
@@ -385,7 +389,44 @@ def verify_attn_lookup_draft(tokens, lens, num_draft, min_match=6, max_match=12,
     return draft, dlen
 
 
+def verify_attn_accept(target_logits, draft_tokens, temperature, seed, draft_logits=None, stream=None):
+    """Speculative acceptance (rejection sampler) after the verify pass:
+    ``target_logits`` fp32 ``[B, T+1, V]``, ``draft_tokens`` int32 ``[B, T]``,
+    ``temperature`` fp32 ``[B]`` (<= 0: greedy), ``draft_logits`` fp32
+    ``[B, T, V]`` or None (a point-mass proposal, as for lookup drafts), all
+    CUDA tensors; ``seed`` picks the Philox stream.  Returns (out_tokens int32
+    ``[B, T+1]`` with -1 after the emitted token, num_accepted int32 ``[B]``)."""
+    import torch
+    if target_logits.dim() != 3 or draft_tokens.dim() != 2:
+        raise ValueError("target_logits must be [B, T+1, V] and draft_tokens [B, T]")
+    B, T1, V = target_logits.shape
+    T = T1 - 1
+    if tuple(draft_tokens.shape) != (B, T):
+        raise ValueError("draft_tokens must be [B, T]")
+    if draft_logits is not None and tuple(draft_logits.shape) != (B, T, V):
+        raise ValueError("draft_logits must be [B, T, V]")
+    f32, i32 = (torch.float32,), (torch.int32,)
+    zp = _dev_ptr(target_logits, "target_logits", f32)
+    wp = _dev_ptr(draft_logits, "draft_logits", f32, allow_none=True)
+    dp = _dev_ptr(draft_tokens, "draft_tokens", i32)
+    tp = _dev_ptr(temperature, "temperature", f32)
+    lib = _load()
+    ws = torch.empty(max(16, int(lib.verify_attn_accept_workspace_bytes(int(B), int(T)))), dtype=torch.uint8,
+                     device=target_logits.device)
+    out = torch.empty((B, T1), dtype=torch.int32, device=target_logits.device)
+    nacc = torch.empty((B,), dtype=torch.int32, device=target_logits.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(target_logits.device)
+    st = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    rc = lib.verify_attn_accept(zp, wp, dp, tp, int(B), int(T), int(V), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                ctypes.c_void_p(nacc.data_ptr()), st)
+    _check(rc, "verify_attn_accept")
+    return out, nacc
+
+
 __all__ = [
+    "verify_attn_accept",
     "verify_attn_lookup_draft",
     "verify_attn_kv_append",
     "verify_attn_noalloc",

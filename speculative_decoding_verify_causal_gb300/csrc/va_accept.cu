@@ -1,0 +1,318 @@
+// Speculative acceptance after the verify pass (the rejection sampler).
+// Definition in verify_attn.h: greedy prefix match; sampled positions accept
+// d[t] iff u q(d) < p(d) (q a point mass for lookup drafts, softmax of the raw
+// draft logits with the temperature applied once otherwise); the first
+// rejection emits a sample of max(0, p - q), a full acceptance the bonus
+// sample of p_T, both as exponential races with Philox4x32-10 Gumbel variates.
+//
+// Two kernels, each a thread-block cluster of kCluster CTAs splitting the
+// vocabulary into slices, partial results exchanged through distributed
+// shared memory (combined in rank order, so every CTA and every run gets the
+// same binary32 value).  stats_kernel, one cluster per (sequence, position):
+// the maximum and argmax of z / tau (of z when greedy), the log-sum-exp and
+// p(d), and the same for the draft logits.  decide_kernel, one cluster per
+// sequence: every CTA walks the positions with those statistics (the same
+// uniforms, so the same decision), then the cluster runs the one race the
+// sequence needs.  Each vocabulary row is read once per pass, fp32,
+// coalesced.
+#include <math.h>
+
+#include "va_internal.h"
+#include "va_sm100.cuh"
+
+namespace va {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 1024;
+constexpr int kCluster = 8;  // CTAs per vocabulary row (portable cluster size)
+
+struct PosStats {  // one (sequence, position); 32 bytes
+    float lse_p, p_d, q_d, lse_q;
+    int argmax, pad[3];
+};
+
+struct AcceptParams {
+    const float *z;       // [B, T+1, V]
+    const float *w;       // [B, T, V] or null
+    const int32_t *d;     // [B, T]
+    const float *tau;     // [B]
+    PosStats *stats;      // [B, T+1]
+    int32_t *out;         // [B, T+1]
+    int32_t *nacc;        // [B]
+    unsigned long long seed;
+    int B, T, V;
+};
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32
+// multiplies, the key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint32_t philox_first_word(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                      uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// U(b, t, i, k) in (0, 1): 24 bits of the first Philox word, centred.
+__device__ __forceinline__ float uniform01(const AcceptParams &p, int b, int t, int i, int k) {
+    const uint32_t w = philox_first_word((uint32_t)i, (uint32_t)t, (uint32_t)b, (uint32_t)k, (uint32_t)p.seed,
+                                         (uint32_t)(p.seed >> 32));
+    return ((float)(w >> 8) + 0.5f) * 5.9604644775390625e-8f;  // 2^-24
+}
+
+// Order-preserving map of a float to uint32 (larger float, larger code).
+__device__ __forceinline__ uint32_t ordered(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float unordered(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// key = (ordered value, smallest index wins ties)
+__device__ __forceinline__ unsigned long long vkey(float v, int i) {
+    return ((unsigned long long)ordered(v) << 32) | (0xFFFFFFFFu - (uint32_t)i);
+}
+
+__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, v, o);
+        v = x > v ? x : v;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red may still be read by a previous reduction
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, v, o);
+        v = x > v ? x : v;
+    }
+    return v;
+}
+
+__device__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Cluster-wide max of one 64-bit key per CTA (slot: this CTA's shared word).
+__device__ unsigned long long cluster_max_u64(unsigned long long v, unsigned long long *slot) {
+    if (threadIdx.x == 0) *slot = v;
+    cluster_sync();
+    unsigned long long m = 0;
+    const uint32_t n = cluster_size();
+    for (uint32_t r = 0; r < n; ++r) {
+        const unsigned long long x = ld_cluster_u64(slot, r);
+        m = x > m ? x : m;
+    }
+    cluster_sync();  // slots may be rewritten after this
+    return m;
+}
+
+// Cluster-wide sum of one float per CTA, added in rank order.
+__device__ float cluster_sum(float v, float *slot) {
+    if (threadIdx.x == 0) *slot = v;
+    cluster_sync();
+    float s = 0.f;
+    const uint32_t n = cluster_size();
+    for (uint32_t r = 0; r < n; ++r) s += ld_cluster_f32(slot, r);
+    cluster_sync();
+    return s;
+}
+
+// This CTA's slice [lo, hi) of a V-long row.
+__device__ __forceinline__ void slice(int V, int &lo, int &hi) {
+    const int r = (int)cluster_rank(), n = (int)cluster_size();
+    const int per = (V + n - 1) / n;
+    lo = min(V, r * per);
+    hi = min(V, lo + per);
+}
+
+// Row statistics over the cluster: max (and its smallest index) of row * scale,
+// and the log-sum-exp of row * scale when want_lse.
+__device__ void row_stats(const float *row, int V, float scale, bool want_lse, unsigned long long *redk,
+                          float *redf, unsigned long long *slot_k, float *slot_f, float &lse, int &argmax) {
+    int lo, hi;
+    slice(V, lo, hi);
+    unsigned long long k = 0;
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        const unsigned long long c = vkey(row[i] * scale, i);
+        k = c > k ? c : k;
+    }
+    k = cluster_max_u64(block_max_u64(k, redk), slot_k);
+    argmax = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+    if (!want_lse) return;
+    const float m = unordered((uint32_t)(k >> 32));
+    float s = 0.f;
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) s += expf(row[i] * scale - m);
+    s = cluster_sum(block_sum(s, redf), slot_f);
+    lse = m + logf(s);
+}
+
+__global__ void __launch_bounds__(kThreads) stats_kernel(const AcceptParams p) {
+    __shared__ unsigned long long redk[kThreads / 32];
+    __shared__ float redf[kThreads / 32];
+    __shared__ unsigned long long slot_k;
+    __shared__ float slot_f;
+    griddep_wait();
+    const int t = blockIdx.y, b = blockIdx.z;
+    const float tau = p.tau[b];
+    const bool greedy = !(tau > 0.f);
+    const float inv = greedy ? 1.f : 1.f / tau;
+    const float *z = p.z + ((size_t)b * (p.T + 1) + t) * p.V;
+    PosStats st{};
+    row_stats(z, p.V, inv, !greedy, redk, redf, &slot_k, &slot_f, st.lse_p, st.argmax);
+    if (!greedy && t < p.T) {
+        const int d = p.d[(size_t)b * p.T + t];
+        const bool valid = d >= 0 && d < p.V;
+        st.p_d = valid ? expf(z[d] * inv - st.lse_p) : 0.f;
+        if (p.w) {
+            const float *w = p.w + ((size_t)b * p.T + t) * p.V;
+            int am;
+            row_stats(w, p.V, inv, true, redk, redf, &slot_k, &slot_f, st.lse_q, am);
+            st.q_d = valid ? expf(w[d] * inv - st.lse_q) : 0.f;
+        } else {
+            st.q_d = valid ? 1.f : 0.f;
+        }
+    }
+    if (cluster_rank() == 0 && threadIdx.x == 0) p.stats[(size_t)b * (p.T + 1) + t] = st;
+}
+
+__global__ void __launch_bounds__(kThreads) decide_kernel(const AcceptParams p) {
+    __shared__ unsigned long long redk[kThreads / 32];
+    __shared__ unsigned long long slot_k;
+    __shared__ int s_n;
+    griddep_wait();
+    const int b = blockIdx.y;
+    const float tau = p.tau[b];
+    const bool greedy = !(tau > 0.f);
+    const PosStats *st = p.stats + (size_t)b * (p.T + 1);
+    const int32_t *d = p.d + (size_t)b * p.T;
+    if (threadIdx.x == 0) {  // every CTA of the cluster takes the same decision
+        int n = p.T;
+        for (int t = 0; t < p.T; ++t) {
+            const bool valid = d[t] >= 0 && d[t] < p.V;
+            const bool ok = greedy ? (valid && d[t] == st[t].argmax)
+                                   : (valid && uniform01(p, b, t, 0, 0) * st[t].q_d < st[t].p_d);
+            if (!ok) {
+                n = t;
+                break;
+            }
+        }
+        s_n = n;
+    }
+    __syncthreads();
+    const int n = s_n;
+    int tok = 0;
+    if (greedy) {
+        tok = st[n].argmax;
+    } else {
+        const float inv = 1.f / tau;
+        const float *z = p.z + ((size_t)b * (p.T + 1) + n) * p.V;
+        const bool bonus = n == p.T;
+        const int dn = bonus ? -1 : d[n];
+        const float *w = (!bonus && p.w) ? p.w + ((size_t)b * p.T + n) * p.V : nullptr;
+        int lo, hi;
+        slice(p.V, lo, hi);
+        unsigned long long k = 0;
+        for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+            const float g = -logf(-logf(uniform01(p, b, n, i, 1)));
+            float score;
+            if (w) {
+                const float r = expf(z[i] * inv - st[n].lse_p) - expf(w[i] * inv - st[n].lse_q);
+                score = r > 0.f ? logf(r) + g : -INFINITY;
+            } else {
+                score = i == dn ? -INFINITY : z[i] * inv + g;
+            }
+            const unsigned long long c = vkey(score, i);
+            k = c > k ? c : k;
+        }
+        k = cluster_max_u64(block_max_u64(k, redk), &slot_k);
+        tok = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+    }
+    if (cluster_rank() == 0) {
+        for (int t = threadIdx.x; t <= p.T; t += blockDim.x)
+            p.out[(size_t)b * (p.T + 1) + t] = t < n ? d[t] : (t == n ? tok : -1);
+        if (threadIdx.x == 0) p.nacc[b] = n;
+    }
+}
+
+// Launch with a (kCluster, 1, 1) cluster and programmatic dependent launch.
+template <typename K>
+cudaError_t launch_cluster(K kernel, dim3 grid, cudaStream_t s, const AcceptParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace
+}  // namespace va
+
+extern "C" size_t verify_attn_accept_workspace_bytes(int num_seqs, int T) {
+    if (num_seqs < 1 || T < 1) return 0;
+    return sizeof(va::PosStats) * (size_t)num_seqs * (size_t)(T + 1);
+}
+
+extern "C" int verify_attn_accept(const float *target_logits, const float *draft_logits,
+                                  const int32_t *draft_tokens, const float *temperature, int num_seqs, int T,
+                                  int vocab, uint64_t seed, void *workspace, int32_t *out_tokens,
+                                  int32_t *num_accepted, void *stream) {
+    if (!target_logits || !draft_tokens || !temperature || !workspace || !out_tokens || !num_accepted)
+        return VA_ERR_INVALID_ARGUMENT;
+    if (num_seqs < 1 || num_seqs > 65535 || T < 1 || T > 65535 || vocab < 1) return VA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return VA_ERR_INVALID_ARGUMENT;
+    va::AcceptParams p{};
+    p.z = target_logits;
+    p.w = draft_logits;
+    p.d = draft_tokens;
+    p.tau = temperature;
+    p.stats = static_cast<va::PosStats *>(workspace);
+    p.out = out_tokens;
+    p.nacc = num_accepted;
+    p.seed = seed;
+    p.B = num_seqs;
+    p.T = T;
+    p.V = vocab;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = va::launch_cluster(va::stats_kernel, dim3(va::kCluster, T + 1, num_seqs), s, p);
+    if (e == cudaSuccess) e = va::launch_cluster(va::decide_kernel, dim3(va::kCluster, num_seqs), s, p);
+    if (e != cudaSuccess) {
+        va::note_cuda_error(e);
+        return VA_ERR_CUDA;
+    }
+    return VA_OK;
+}

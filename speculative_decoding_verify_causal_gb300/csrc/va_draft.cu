@@ -14,9 +14,12 @@
 #include <algorithm>
 
 #include "va_internal.h"
+#include "va_sm100.cuh"
 
 namespace va {
 namespace {
+
+using namespace sm100;
 
 constexpr int kThreads = 1024;
 constexpr int kMaxMatch = 32;
@@ -29,33 +32,6 @@ struct DraftParams {
     int32_t *draft, *draft_len, *match_end, *match_len;
     int stride, min_match, max_match, num_draft;
 };
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t n;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-    return n;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 64-bit load from the shared memory of CTA `rank` of this cluster, at the
-// address `local` has in this CTA.
-__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, uint32_t rank) {
-    uint32_t remote;
-    const uint32_t addr = (uint32_t)__cvta_generic_to_shared(local);
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll

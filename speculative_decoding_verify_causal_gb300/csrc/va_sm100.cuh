@@ -269,6 +269,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// ----------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+// Barrier over every thread of every CTA of the cluster, with release /
+// acquire ordering of shared-memory writes across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in CTA `rank`'s shared memory of the object at `local` in this CTA.
+__device__ __forceinline__ uint32_t cluster_map(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, uint32_t rank) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_map(local, rank)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(const void *local, uint32_t rank) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_map(local, rank)) : "memory");
+    return v;
+}
+
 // ----------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets in 16-byte units, descriptor version 1 at bits 46-47,
