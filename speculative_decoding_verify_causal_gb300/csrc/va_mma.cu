@@ -386,8 +386,10 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             int issued = 0;
             for (int ps = 0; ps < npass; ++ps) {
                 const int slot = ps % nst, use = ps / nst;
-                ok = __shfl_sync(0xffffffffu, (int)mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs), 0);
-                if (!ok) break;
+                if (use > 0) {  // a slot's first use needs no wait
+                    ok = __shfl_sync(0xffffffffu, (int)mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs), 0);
+                    if (!ok) break;
+                }
                 const int i = ps >> 1, kv = ps & 1;
                 const int npg = tile_npg(i);
                 const int page = tile_page(i);
