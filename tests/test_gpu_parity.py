@@ -69,6 +69,23 @@ def test_full_size_configs_sampled_rows(name):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+# ------------------------------------------------------------ long contexts, other dtypes / widths
+@pytest.mark.parametrize("D,dt,L,T,G", [(128, "bf16", 20_000, 8, 6), (64, "fp8_e4m3", 30_000, 5, 8),
+                                        (256, "bf16", 12_000, 16, 6), (128, "int8", 40_000, 16, 4)])
+def test_long_context_other_shapes_sampled_rows(D, dt, L, T, G):
+    """The tensor-core path well past one split per SM in the other head
+    widths and cache types (sampled rows against the oracle, all outputs finite)."""
+    w = wl.make_workload(7000 + D + L, [L], T, G * 2, 2, D, dt)
+    out, lse, info = run_gpu(w)
+    assert info["path"] == 2 and info["max_splits"] > 1
+    rows = _sample_rows(w, n_extra=10)
+    ref_o, ref_l = oracle.verify_attn_rows(w, rows)
+    got_o = np.stack([out[b, t, h] for b, t, h in rows])
+    got_l = np.array([lse[b, t, h] for b, t, h in rows])
+    compare(got_o, got_l, ref_o, ref_l, f"D{D} {dt} L{L} {info}")
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
 # ------------------------------------------------------------ shape sweep
 SWEEP = []
 for T in (1, 5, 8, 16):
