@@ -13,9 +13,10 @@ through enough independent cache copies that every call reads its KV from
 HBM.  Steps are replayed from a CUDA graph so that launch overhead does not
 pace the GPU.
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
-the host cores instead (the reference arm of this build: there is no other
-implementation to run).
+Prints ONE JSON line (rank 0).  Besides the verify figures the line carries
+separate timings of the steps around it (KV append, lookup drafting,
+acceptance).  ``--impl reference`` times the CPU oracle on the host cores
+instead: the method has no other implementation to compare against.
 """
 from __future__ import annotations
 

@@ -204,8 +204,8 @@ const char *verify_attn_last_cuda_error_string(void);
  * call cudaMalloc: code running where the allocator is off limits (inside a
  * custom memory pool's accounting, a real-time or signal-safe path, or an
  * embedding runtime that owns all device memory), or that must not grow the
- * device footprint after start-up.  (The paper has no counterpart: this entry
- * exists for deployment.)
+ * device footprint after start-up.  (The method's sources describe no such
+ * entry: it exists for deployment.)
  *
  * It plans from seq_lens_host on every call (host work only, no heap) and
  * keeps the work list and the split partials in a static device array of
