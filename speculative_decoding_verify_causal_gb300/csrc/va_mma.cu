@@ -13,22 +13,27 @@
 // read from HBM".
 //
 // Per 64-key tile (4 pages):
-//   producer warp    TMA-gathers the pages named by the block table (4-D
-//                    tensor map over [page, slot, kv head, d]) plus the
-//                    pages' scale blocks (1-D bulk copies);
-//   dequant warps    (fp8-e4m3 / int8) convert the raw bytes to fp16 -- both
-//                    conversions are exact -- into the 128-byte-swizzled
-//                    layout the MMA reads (bf16 caches are TMA'd straight
-//                    into that layout);
+//   producer warp    stages the item's page ids, then TMA-gathers the pages
+//                    named by the block table (4-D tensor map over [page,
+//                    slot, kv head, d], one box per page) into a ring of raw
+//                    stages, K then V of every tile;
+//   dequant warps    (fp8-e4m3 / int8) take a raw stage into registers, hand
+//                    it back, and write fp16 -- both conversions are exact --
+//                    into the 128-byte-swizzled layout the MMA reads; they
+//                    also carry each key's k and v scale (loaded two tiles
+//                    ahead) into a ring the softmax reads (bf16 caches are
+//                    TMA'd straight into the MMA layout);
 //   MMA warp         one thread issues S = Q K^T (A = Q in TMEM, B = K tile in
 //                    shared memory, D = S in TMEM, M=128 N=64 K=16 x D/16) and
 //                    O += P V (A = P in TMEM, B = V tile, N = D);
-//   softmax warps    one thread per packed row: reads its S row from TMEM,
-//                    applies the per-key k scale and the bottom-right causal
-//                    mask, keeps the running max / sum (base 2; the max is
-//                    only moved, and O rescaled, when it grows by more than
-//                    2^8), writes P * v_scale (fp16) back over S in TMEM,
-//                    and at the end writes O / l and the log-sum-exp.
+//   softmax warps    two per TMEM lane quarter (one thread per packed row and
+//                    half of the tile's keys): read S from TMEM, apply the
+//                    per-key k scale and the bottom-right causal mask, keep the
+//                    running max / sum (base 2; the max is only moved, and O
+//                    rescaled, when it grows by more than 2^8), write
+//                    P * v_scale (fp16) back over S in TMEM, and at the end
+//                    write O / l and the log-sum-exp (split partials leave by
+//                    TMA box stores).
 // Scales are constant along head_dim, so dequantisation is an exact cast
 // and the scales are folded into the scores (k) and into P (v).
 //
