@@ -83,8 +83,8 @@ struct Cfg {
     static constexpr int kConvBytes = kTile * D * 2;   // K or V tile, 16-bit, SW128 chunks of 64 d
     static constexpr int kChunkBytes = kTile * 128;    // one 64-d chunk of a tile
     static constexpr int kRawTileBytes = kTile * D;    // one K or V tile, 8-bit
-    // warps 0-7 softmax (two per TMEM lane quarter), 8-11 dequant (quantised
-    // caches only), then the producer and the MMA issuer
+    // warps 0-7 softmax (two per TMEM lane quarter), 8-15 dequant (quantised
+    // caches only: 8-11 K, 12-15 V), then the producer and the MMA issuer
     static constexpr int kSoftmaxWarps = 8;
     static constexpr int kDequantWarps = kQuant ? 8 : 0;
     static constexpr int kProducerWarp = kSoftmaxWarps + kDequantWarps;
@@ -238,11 +238,11 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             prefetch_tensormap(&mp.tm_v);
             for (int i = 0; i < kMaxRawStages; ++i) {
                 mbar_init(bar(kRawFull + i), 1);
-                mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps : 1);
+                mbar_init(bar(kRawEmpty + i), C::kQuant ? C::kDequantWarps / 2 : 1);  // one dequant group
             }
             for (int i = 0; i < 3; ++i) {
-                mbar_init(bar(kKFull + i), C::kQuant ? C::kDequantWarps : 1);
-                mbar_init(bar(kVFull + i), C::kQuant ? C::kDequantWarps : 1);
+                mbar_init(bar(kKFull + i), C::kQuant ? C::kDequantWarps / 2 : 1);
+                mbar_init(bar(kVFull + i), C::kQuant ? C::kDequantWarps / 2 : 1);
                 mbar_init(bar(kKEmpty + i), 1);
                 mbar_init(bar(kVEmpty + i), 1);
             }
@@ -760,50 +760,50 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         }
     } else if constexpr (C::kQuant) {
         // ------------------------------------------------------------ dequant
-        // One pass per raw stage: the K tile (plus this head's k and v scales,
-        // which the softmax of the tile needs) or the V tile, int8 / e4m3 ->
+        // Two groups of four warps, one per lane quarter each: warps 8-11 take
+        // the K tile of every tile (plus this head's k and v scales, which the
+        // softmax of the tile needs), warps 12-15 the V tile, so that the K
+        // pass of tile i+1 runs beside the V pass of tile i.  int8 / e4m3 ->
         // fp16 (exact) into the MMA layout.
-        constexpr int kDT = C::kDequantWarps * 32;
-        const int dt = tid - C::kSoftmaxWarps * 32;  // 0 .. kDT-1
+        constexpr int kGT = C::kDequantWarps * 16;             // threads per group
+        const int dq = tid - C::kSoftmaxWarps * 32;            // 0 .. 2 kGT - 1
+        const int kv = dq / kGT;                               // 0: K group, 1: V group
+        const int dt = dq % kGT;
         const uint32_t ring = sbase + L.scale_ring;
-        constexpr int kChunks = kTile * D / 16;      // 16-byte raw chunks per tile
-        constexpr int kPer = kChunks / kDT;          // per thread (1, 2 or 4)
-        static_assert(kPer * kDT == kChunks, "chunks must divide evenly");
-        // this thread's chunks: raw byte offset, tile row and destinations of
-        // its two 16-byte fp16 units (store order alternates between 64-d
+        constexpr int kChunks = kTile * D / 16;                // 16-byte raw chunks per tile
+        constexpr int kPer = kChunks / kGT;                    // per thread (2, 4 or 8)
+        constexpr int kRowStep = kGT * 16 / D;                 // tile rows between a thread's chunks
+        static_assert(kPer * kGT == kChunks && kRowStep % 8 == 0, "chunks must divide evenly");
+        // this thread's chunks sit kGT * 16 raw bytes (kRowStep rows, a
+        // multiple of the swizzle period) apart; destinations of the first
+        // chunk's two 16-byte fp16 units (store order alternates between 64-d
         // chunks so that a quarter-warp never hits a bank twice)
-        uint32_t roff[kPer], woff_lo[kPer], woff_hi[kPer];
-        int row_of[kPer];
-#pragma unroll
-        for (int jj = 0; jj < kPer; ++jj) {
-            const int q = dt + kDT * jj;
-            const int n = q * 16 / D, d0 = (q * 16) % D;
-            const int c = d0 / 64, u0 = (d0 % 64) / 8;
-            roff[jj] = q * 16;
-            row_of[jj] = n;
-            woff_lo[jj] = c * C::kChunkBytes + sw128(n, u0);
-            woff_hi[jj] = c * C::kChunkBytes + sw128(n, u0 + 1);
-        }
-        const bool odd_chunk = ((dt * 16 % D) / 64) & 1;  // same parity for every jj (kDT*16 % 128 == 0)
-        // threads dt < 128 carry one scale of a tile: k (dt < 64) or v of key
-        // dt % 64, loaded from global two tiles before it is needed
+        const int n0 = dt * 16 / D, d0 = (dt * 16) % D;
+        const uint32_t woff_lo = (d0 / 64) * C::kChunkBytes + sw128(n0, (d0 % 64) / 8);
+        const uint32_t woff_hi = (d0 / 64) * C::kChunkBytes + sw128(n0, (d0 % 64) / 8 + 1);
+        const bool odd_chunk = (d0 / 64) & 1;
+        // K group: thread dt carries one scale of a tile, k (dt < 64) or v of
+        // key dt % 64, loaded from global two tiles before it is needed
+        static_assert(kGT == 2 * kTile, "one scale per K-group thread");
         const float *scale_src = dt < kTile ? p.k_scale : p.v_scale;
         auto load_scale = [&](int i) -> float {
             const int n = dt % kTile;
             const int key = it.k_begin + i * kTile + n;
-            if (dt >= 2 * kTile || i >= ntiles || key >= it.k_end) return 0.f;
+            if (i >= ntiles || key >= it.k_end) return 0.f;
             const int page = (int)lds_u32(sbase + L.pids + 4u * (i * (kTile / VA_PAGE_SIZE) + n / VA_PAGE_SIZE));
             return __ldg(scale_src + ((size_t)page * VA_PAGE_SIZE + n % VA_PAGE_SIZE) * Hkv + it.kvh);
         };
         // two tiles of scales in flight: a global load under load takes about as
         // long as a tile
-        float scale_cur = load_scale(0), scale_nxt = load_scale(1);
-        const int npass = 2 * ntiles;
-        for (int ps = 0; ps < npass && ok; ++ps) {
-            const int i = ps >> 1, kv = ps & 1;
+        float scale_cur = 0.f, scale_nxt = 0.f;
+        if (kv == 0) {
+            scale_cur = load_scale(0);
+            scale_nxt = load_scale(1);
+        }
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int ps = 2 * i + kv;  // raw passes: K of tile 0, V of tile 0, K of tile 1, ...
             const int buf = i % C::kNumBuf, use = i / C::kNumBuf;
-            const int key0 = it.k_begin + i * kTile;
-            const int nvalid = min(kTile, it.k_end - key0);
+            const int nvalid = min(kTile, it.k_end - (it.k_begin + i * kTile));
             const int slot = ps % nst;
             // the raw bytes go to registers and the stage is handed back to
             // the producer at once, before waiting for the fp16 buffer
@@ -811,15 +811,15 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 ok = false;
                 break;
             }
-            const uint32_t st = sbase + L.raw + slot * L.raw_stride;
+            const uint32_t st = sbase + L.raw + slot * L.raw_stride + dt * 16;
             const uint32_t dst = sbase + (kv == 0 ? L.conv_k : L.conv_v) + buf * C::kConvBytes;
             uint4 raw[kPer];
 #pragma unroll
-            for (int jj = 0; jj < kPer; ++jj) raw[jj] = lds_u4(st + roff[jj]);
+            for (int jj = 0; jj < kPer; ++jj) raw[jj] = lds_u4(st + jj * kGT * 16);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kRawEmpty + slot));
-            // K pass: the tile's scales move up the pipeline and the load two
-            // tiles ahead is issued now, before this pass's stores fill the
+            // the tile's scales move up the pipeline and the load two tiles
+            // ahead is issued now, before this pass's stores fill the
             // shared-memory queue
             float scale_out = 0.f;
             if (kv == 0) {
@@ -844,16 +844,17 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 }
                 uint4 lo = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 uint4 hi = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-                if (row_of[jj] >= nvalid) lo = hi = make_uint4(0, 0, 0, 0);  // past the split end
+                if (n0 + jj * kRowStep >= nvalid) lo = hi = make_uint4(0, 0, 0, 0);  // past the split end
+                const uint32_t row_off = jj * kRowStep * 128;
                 if (odd_chunk) {
-                    sts_u4(dst + woff_hi[jj], hi);
-                    sts_u4(dst + woff_lo[jj], lo);
+                    sts_u4(dst + woff_hi + row_off, hi);
+                    sts_u4(dst + woff_lo + row_off, lo);
                 } else {
-                    sts_u4(dst + woff_lo[jj], lo);
-                    sts_u4(dst + woff_hi[jj], hi);
+                    sts_u4(dst + woff_lo + row_off, lo);
+                    sts_u4(dst + woff_hi + row_off, hi);
                 }
             }
-            if (kv == 0 && dt < 2 * kTile) {  // the tile's k and v scales (zero past the end) -> ring
+            if (kv == 0) {  // the tile's k and v scales (zero past the end) -> ring
                 // slot i % kScaleRing held tile i - kScaleRing, whose softmax has to have read it
                 if (!mbar_wait(bar(kRingFree + i % kScaleRing), ((i / kScaleRing) & 1) ^ 1, kWaitNs)) ok = false;
                 sts_f32(ring + (i % kScaleRing) * 2 * kTile * 4 + 4u * dt, scale_out);
