@@ -153,6 +153,39 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Packed fp32 pairs (sm_100+): each lane of a pair is one IEEE-rounded fp32
+// multiply / fused multiply-add / add, the same result as the scalar
+// instruction, at half the issue cost.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, uint32_t &lo, uint32_t &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -554,16 +587,16 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        if (C::kQuant) {
-                            const float4 sc = lds_f4(ks + 16 * j4);
-                            s[4 * j4 + 0] = __float_as_uint(__uint_as_float(s[4 * j4 + 0]) * sc.x);
-                            s[4 * j4 + 1] = __float_as_uint(__uint_as_float(s[4 * j4 + 1]) * sc.y);
-                            s[4 * j4 + 2] = __float_as_uint(__uint_as_float(s[4 * j4 + 2]) * sc.z);
-                            s[4 * j4 + 3] = __float_as_uint(__uint_as_float(s[4 * j4 + 3]) * sc.w);
+                        if (C::kQuant) {  // k scales: two packed multiplies per four keys
+                            const uint4 sc = lds_u4(ks + 16 * j4);
+                            f2_unpack(f2_mul(f2_pack(s[4 * j4], s[4 * j4 + 1]), f2_pack(sc.x, sc.y)), s[4 * j4],
+                                      s[4 * j4 + 1]);
+                            f2_unpack(f2_mul(f2_pack(s[4 * j4 + 2], s[4 * j4 + 3]), f2_pack(sc.z, sc.w)),
+                                      s[4 * j4 + 2], s[4 * j4 + 3]);
                         }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            mx[(4 * j4 + e) & 7] = fmaxf(mx[(4 * j4 + e) & 7], __uint_as_float(s[4 * j4 + e]));
+                        const int c = j4 & 3;  // four chains of three-input maxima
+                        mx[c] = fmax3(mx[c], __uint_as_float(s[4 * j4]), __uint_as_float(s[4 * j4 + 1]));
+                        mx[c] = fmax3(mx[c], __uint_as_float(s[4 * j4 + 2]), __uint_as_float(s[4 * j4 + 3]));
                     }
                 } else {
 #pragma unroll
@@ -583,8 +616,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         }
                     }
                 }
-                float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmaxf(mx[5], fmaxf(mx[6], mx[7]))));
                 // exchange with the other half (double-buffered by tile parity)
                 sts_f32(xmax + 4u * ((b * 2 + half) * 128 + r), mt);
                 named_bar_sync(pair_bar, 64);
@@ -617,25 +649,35 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 // p = 2^(x*c - m); masked keys give 2^-inf = 0 and carry a zero
                 // v scale, so no select is needed
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+                const uint64_t c2 = f2_pack(__float_as_uint(c_r), __float_as_uint(c_r));
+                const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
                 uint32_t pk[16];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                uint64_t ls[2] = {0ull, 0ull};  // packed partial sums (+0.0f pairs)
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 0]), c_r, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 1]), c_r, neg_m));
-                    const float p2 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 2]), c_r, neg_m));
-                    const float p3 = ex2_approx(fmaf(__uint_as_float(s[4 * j4 + 3]), c_r, neg_m));
-                    ls[j4 & 3] += (p0 + p1) + (p2 + p3);
+                    uint32_t a[4];
+                    f2_unpack(f2_fma(f2_pack(s[4 * j4], s[4 * j4 + 1]), c2, nm2), a[0], a[1]);
+                    f2_unpack(f2_fma(f2_pack(s[4 * j4 + 2], s[4 * j4 + 3]), c2, nm2), a[2], a[3]);
+                    uint32_t pb[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) pb[e] = __float_as_uint(ex2_approx(__uint_as_float(a[e])));
+                    const uint64_t p01 = f2_pack(pb[0], pb[1]), p23 = f2_pack(pb[2], pb[3]);
+                    ls[j4 & 1] = f2_add(ls[j4 & 1], f2_add(p01, p23));
                     if (C::kQuant) {
-                        const float4 sc = lds_f4(vs + 16 * j4);
-                        pk[2 * j4] = pack_half2(p0 * sc.x, p1 * sc.y);
-                        pk[2 * j4 + 1] = pack_half2(p2 * sc.z, p3 * sc.w);
+                        const uint4 sc = lds_u4(vs + 16 * j4);
+                        uint32_t w[4];
+                        f2_unpack(f2_mul(p01, f2_pack(sc.x, sc.y)), w[0], w[1]);
+                        f2_unpack(f2_mul(p23, f2_pack(sc.z, sc.w)), w[2], w[3]);
+                        pk[2 * j4] = pack_half2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                        pk[2 * j4 + 1] = pack_half2(__uint_as_float(w[2]), __uint_as_float(w[3]));
                     } else {
-                        pk[2 * j4] = pack_bf162(p0, p1);
-                        pk[2 * j4 + 1] = pack_bf162(p2, p3);
+                        pk[2 * j4] = pack_bf162(__uint_as_float(pb[0]), __uint_as_float(pb[1]));
+                        pk[2 * j4 + 1] = pack_bf162(__uint_as_float(pb[2]), __uint_as_float(pb[3]));
                     }
                 }
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                uint32_t l0, l1;
+                f2_unpack(f2_add(ls[0], ls[1]), l0, l1);
+                l_run += __uint_as_float(l0) + __uint_as_float(l1);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kRingFree + i % kScaleRing));  // scale slot read
                 // P row r, keys [32 half, 32 half + 32) -> columns [16 half, 16 half + 16)
