@@ -255,6 +255,26 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
 
     const int lp0 = it.k_begin / VA_PAGE_SIZE;                               // first logical page
     const int npages_item = (it.k_end + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE - lp0;
+    // producer: lane pg < 4 issues the TMA box of page pg of a tile (page ids
+    // from shared memory, 0 past the end); one raw stage per K or V pass
+    auto tile_page = [&](int i) -> int {
+        const int k = i * (kTile / VA_PAGE_SIZE) + lane;
+        return (lane < kTile / VA_PAGE_SIZE && k < npages_item) ? (int)lds_u32(sbase + L.pids + 4u * k) : 0;
+    };
+    auto tile_npg = [&](int i) { return min(kTile / VA_PAGE_SIZE, npages_item - i * (kTile / VA_PAGE_SIZE)); };
+    auto issue_raw = [&](int ps) {
+        const int slot = ps % nst, i = ps >> 1, kv = ps & 1;
+        const int npg = tile_npg(i);
+        const int page = tile_page(i);
+        const uint32_t page_bytes = VA_PAGE_SIZE * D;  // one page, one head, 8-bit
+        if (lane == 0) mbar_arrive_expect_tx(bar(kRawFull + slot), npg * page_bytes);
+        __syncwarp();
+        if (lane < npg)
+            tma_load_4d(sbase + L.raw + slot * L.raw_stride + lane * page_bytes, kv == 0 ? &mp.tm_k : &mp.tm_v, 0,
+                        it.kvh, 0, page, bar(kRawFull + slot));
+        __syncwarp();
+    };
+    int pre_issued = 0;  // raw stages the producer issued during set-up
     if (warp == C::kProducerWarp) {
         // Set-up by the producer warp, which then arrives at the set-up
         // barrier without waiting for the others: its first copies go out
@@ -312,6 +332,12 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         }
         __syncwarp();
         named_bar_arrive(kSetupBar, C::kThreads);
+        // the first stages (each slot's first use needs no wait) go out now,
+        // while the other warps load Q
+        if constexpr (C::kQuant) {
+            pre_issued = min(nst, 2 * ntiles);
+            for (int ps = 0; ps < pre_issued; ++ps) issue_raw(ps);
+        }
     } else if (warp == C::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
@@ -409,35 +435,17 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
 
     if (warp == C::kProducerWarp) {
         // ------------------------------------------------------------ producer
-        // The whole warp walks the stages; lane pg issues the TMA box of the
-        // tile's page pg (page ids come from smem, staged at kernel start).
-        auto tile_page = [&](int i) -> int {  // lane pg: page pg of tile i (0 past the end)
-            const int k = i * (kTile / VA_PAGE_SIZE) + lane;
-            return (lane < kTile / VA_PAGE_SIZE && k < npages_item) ? (int)lds_u32(sbase + L.pids + 4u * k) : 0;
-        };
-        auto tile_npg = [&](int i) {
-            return min(kTile / VA_PAGE_SIZE, npages_item - i * (kTile / VA_PAGE_SIZE));
-        };
+        // The whole warp walks the stages (K and V of every tile) after the
+        // ones issued during set-up, each once the dequant group has handed
+        // its slot back.
         if constexpr (C::kQuant) {
-            const int npass = 2 * ntiles;                          // K and V of every tile
-            const uint32_t page_bytes = VA_PAGE_SIZE * D;          // one page, one head, 8-bit
-            int issued = 0;
-            for (int ps = 0; ps < npass; ++ps) {
-                const int slot = ps % nst, use = ps / nst;
-                if (use > 0) {  // a slot's first use needs no wait
-                    ok = __shfl_sync(0xffffffffu, (int)mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs), 0);
-                    if (!ok) break;
-                }
-                const int i = ps >> 1, kv = ps & 1;
-                const int npg = tile_npg(i);
-                const int page = tile_page(i);
-                const uint32_t st = sbase + L.raw + slot * L.raw_stride;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kRawFull + slot), npg * page_bytes);
-                __syncwarp();
-                if (lane < npg)
-                    tma_load_4d(st + lane * page_bytes, kv == 0 ? &mp.tm_k : &mp.tm_v, 0, it.kvh, 0, page,
-                                bar(kRawFull + slot));
-                __syncwarp();
+            const int npass = 2 * ntiles;
+            int issued = pre_issued;
+            for (int ps = pre_issued; ps < npass; ++ps) {
+                const int slot = ps % nst, use = ps / nst;  // use >= 1 here
+                ok = __shfl_sync(0xffffffffu, (int)mbar_wait(bar(kRawEmpty + slot), (use & 1) ^ 1, kWaitNs), 0);
+                if (!ok) break;
+                issue_raw(ps);
                 issued = ps + 1;
             }
             // drain: every issued copy must land before the CTA may exit
