@@ -16,13 +16,16 @@
 //   producer warp    stages the item's page ids, then TMA-gathers the pages
 //                    named by the block table (4-D tensor map over [page,
 //                    slot, kv head, d], one box per page) into a ring of raw
-//                    stages, K then V of every tile;
-//   dequant warps    (fp8-e4m3 / int8) take a raw stage into registers, hand
-//                    it back, and write fp16 -- both conversions are exact --
-//                    into the 128-byte-swizzled layout the MMA reads; they
-//                    also carry each key's k and v scale (loaded two tiles
-//                    ahead) into a ring the softmax reads (bf16 caches are
-//                    TMA'd straight into the MMA layout);
+//                    stages, K then V of every tile (the first stage of each
+//                    slot already during set-up);
+//   dequant warps    (fp8-e4m3 / int8) two groups of four, one taking the K
+//                    tile and one the V tile of every tile: a raw stage goes
+//                    to registers and back to the producer, then fp16 -- both
+//                    conversions are exact -- into the 128-byte-swizzled
+//                    layout the MMA reads; the K group also carries each
+//                    key's k and v scale (loaded two tiles ahead) into a ring
+//                    the softmax reads (bf16 caches are TMA'd straight into
+//                    the MMA layout);
 //   MMA warp         one thread issues S = Q K^T (A = Q in TMEM, B = K tile in
 //                    shared memory, D = S in TMEM, M=128 N=64 K=16 x D/16) and
 //                    O += P V (A = P in TMEM, B = V tile, N = D);
