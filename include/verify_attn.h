@@ -328,7 +328,8 @@ int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int3
  * [num_seqs, T]; temperature fp32 [num_seqs]; out_tokens int32 [num_seqs,
  * T + 1]; num_accepted int32 [num_seqs]; workspace: at least
  * verify_attn_accept_workspace_bytes(num_seqs, T) bytes, 16-byte aligned,
- * owned by the caller.  The decisions are taken in binary32 (the scores,
+ * owned by the caller; its contents need no initialisation, and calls that
+ * share one workspace must be ordered on one stream.  The decisions are taken in binary32 (the scores,
  * exponentials and logarithms of the CUDA math library), so a CPU restatement
  * in another precision agrees except where two scores, or u and p/q, are
  * within a few ulps.  Returns VA_OK when enqueued, VA_ERR_INVALID_ARGUMENT

@@ -5,17 +5,21 @@
 // rejection emits a sample of max(0, p - q), a full acceptance the bonus
 // sample of p_T, both as exponential races with Philox4x32-10 Gumbel variates.
 //
-// Two kernels, each a thread-block cluster of kCluster CTAs splitting the
-// vocabulary into slices, partial results exchanged through distributed
-// shared memory (combined in rank order, so every CTA and every run gets the
-// same binary32 value).  stats_kernel, one cluster per (sequence, position):
-// the maximum and argmax of z / tau (of z when greedy), the log-sum-exp and
-// p(d), and the same for the draft logits.  decide_kernel, one cluster per
-// sequence: every CTA walks the positions with those statistics (the same
-// uniforms, so the same decision), then the cluster runs the one race the
-// sequence needs.  Each vocabulary row is read once per pass, fp32,
-// coalesced.
+// Two kernels.  stats_kernel, one thread-block cluster of kCluster CTAs per
+// (sequence, position), each CTA a slice of the vocabulary, partial results
+// exchanged through distributed shared memory (combined in rank order, so
+// every CTA and every run gets the same binary32 value): the maximum and
+// argmax of z / tau (of z when greedy), the log-sum-exp and p(d), and the
+// same for the draft logits.  decide_kernel, a row of CTAs per sequence:
+// every CTA evaluates all positions with those statistics in parallel (the
+// same uniforms, so the same first rejection n), then each CTA runs the
+// sequence's one race over its slice of the vocabulary and folds its best key
+// into the sequence's slot with a 64-bit atomic maximum (order-free, so the
+// winner does not depend on timing); the last CTA to finish writes the
+// tokens.  Each vocabulary row is read once per pass, fp32, coalesced.
 #include <math.h>
+
+#include <algorithm>
 
 #include "va_internal.h"
 #include "va_sm100.cuh"
@@ -26,11 +30,20 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 1024;
-constexpr int kCluster = 8;  // CTAs per vocabulary row (portable cluster size)
+constexpr int kCluster = 8;          // CTAs per vocabulary row in the statistics (portable cluster size)
+constexpr int kRaceThreads = 256;    // decide_kernel CTA size
+constexpr int kRacePerThread = 4;    // vocabulary entries per race thread (sets the row of CTAs)
+constexpr int kMaxRaceCtas = 1024;
 
 struct PosStats {  // one (sequence, position); 32 bytes
     float lse_p, p_d, q_d, lse_q;
     int argmax, pad[3];
+};
+
+struct SeqSlot {  // one sequence's race, after the PosStats block; 16 bytes
+    unsigned long long key;  // best (score, index) key so far
+    unsigned int done;       // race CTAs finished
+    unsigned int pad;
 };
 
 struct AcceptParams {
@@ -39,6 +52,7 @@ struct AcceptParams {
     const int32_t *d;     // [B, T]
     const float *tau;     // [B]
     PosStats *stats;      // [B, T+1]
+    SeqSlot *slots;       // [B], cleared by stats_kernel
     int32_t *out;         // [B, T+1]
     int32_t *nacc;        // [B]
     unsigned long long seed;
@@ -183,6 +197,7 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const AcceptParams p) {
     const bool greedy = !(tau > 0.f);
     const float inv = greedy ? 1.f : 1.f / tau;
     const float *z = p.z + ((size_t)b * (p.T + 1) + t) * p.V;
+    if (t == 0 && cluster_rank() == 0 && threadIdx.x == 0) p.slots[b] = SeqSlot{};  // for decide_kernel
     PosStats st{};
     row_stats(z, p.V, inv, !greedy, redk, redf, &slot_k, &slot_f, st.lse_p, st.argmax);
     if (!greedy && t < p.T) {
@@ -201,63 +216,71 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const AcceptParams p) {
     if (cluster_rank() == 0 && threadIdx.x == 0) p.stats[(size_t)b * (p.T + 1) + t] = st;
 }
 
-__global__ void __launch_bounds__(kThreads) decide_kernel(const AcceptParams p) {
-    __shared__ unsigned long long redk[kThreads / 32];
-    __shared__ unsigned long long slot_k;
+__device__ void write_tokens(const AcceptParams &p, int b, int n, int tok) {
+    const int32_t *d = p.d + (size_t)b * p.T;
+    for (int t = threadIdx.x; t <= p.T; t += blockDim.x)
+        p.out[(size_t)b * (p.T + 1) + t] = t < n ? d[t] : (t == n ? tok : -1);
+    if (threadIdx.x == 0) p.nacc[b] = n;
+}
+
+__global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams p) {
+    __shared__ unsigned long long redk[kRaceThreads / 32];
     __shared__ int s_n;
+    __shared__ int s_last;
     griddep_wait();
     const int b = blockIdx.y;
     const float tau = p.tau[b];
     const bool greedy = !(tau > 0.f);
     const PosStats *st = p.stats + (size_t)b * (p.T + 1);
     const int32_t *d = p.d + (size_t)b * p.T;
-    if (threadIdx.x == 0) {  // every CTA of the cluster takes the same decision
-        int n = p.T;
-        for (int t = 0; t < p.T; ++t) {
-            const bool valid = d[t] >= 0 && d[t] < p.V;
-            const bool ok = greedy ? (valid && d[t] == st[t].argmax)
-                                   : (valid && uniform01(p, b, t, 0, 0) * st[t].q_d < st[t].p_d);
-            if (!ok) {
-                n = t;
-                break;
-            }
-        }
-        s_n = n;
+    // n = the first position whose draft is rejected (T if none is)
+    if (threadIdx.x == 0) s_n = p.T;
+    __syncthreads();
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+        const bool valid = d[t] >= 0 && d[t] < p.V;
+        const bool ok = greedy ? (valid && d[t] == st[t].argmax)
+                               : (valid && uniform01(p, b, t, 0, 0) * st[t].q_d < st[t].p_d);
+        if (!ok) atomicMin(&s_n, t);
     }
     __syncthreads();
     const int n = s_n;
-    int tok = 0;
     if (greedy) {
-        tok = st[n].argmax;
-    } else {
-        const float inv = 1.f / tau;
-        const float *z = p.z + ((size_t)b * (p.T + 1) + n) * p.V;
-        const bool bonus = n == p.T;
-        const int dn = bonus ? -1 : d[n];
-        const float *w = (!bonus && p.w) ? p.w + ((size_t)b * p.T + n) * p.V : nullptr;
-        int lo, hi;
-        slice(p.V, lo, hi);
-        unsigned long long k = 0;
-        for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-            const float g = -logf(-logf(uniform01(p, b, n, i, 1)));
-            float score;
-            if (w) {
-                const float r = expf(z[i] * inv - st[n].lse_p) - expf(w[i] * inv - st[n].lse_q);
-                score = r > 0.f ? logf(r) + g : -INFINITY;
-            } else {
-                score = i == dn ? -INFINITY : z[i] * inv + g;
-            }
-            const unsigned long long c = vkey(score, i);
-            k = c > k ? c : k;
+        if (blockIdx.x == 0) write_tokens(p, b, n, st[n].argmax);
+        return;
+    }
+    // the race: this CTA's slice of the vocabulary
+    const float inv = 1.f / tau;
+    const float *z = p.z + ((size_t)b * (p.T + 1) + n) * p.V;
+    const bool bonus = n == p.T;
+    const int dn = bonus ? -1 : d[n];
+    const float *w = (!bonus && p.w) ? p.w + ((size_t)b * p.T + n) * p.V : nullptr;
+    const int per = (p.V + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int lo = min(p.V, (int)blockIdx.x * per), hi = min(p.V, lo + per);
+    unsigned long long k = 0;
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        const float g = -logf(-logf(uniform01(p, b, n, i, 1)));
+        float score;
+        if (w) {
+            const float r = expf(z[i] * inv - st[n].lse_p) - expf(w[i] * inv - st[n].lse_q);
+            score = r > 0.f ? logf(r) + g : -INFINITY;
+        } else {
+            score = i == dn ? -INFINITY : z[i] * inv + g;
         }
-        k = cluster_max_u64(block_max_u64(k, redk), &slot_k);
-        tok = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+        const unsigned long long c = vkey(score, i);
+        k = c > k ? c : k;
     }
-    if (cluster_rank() == 0) {
-        for (int t = threadIdx.x; t <= p.T; t += blockDim.x)
-            p.out[(size_t)b * (p.T + 1) + t] = t < n ? d[t] : (t == n ? tok : -1);
-        if (threadIdx.x == 0) p.nacc[b] = n;
+    k = block_max_u64(k, redk);
+    SeqSlot *slot = p.slots + b;
+    if (threadIdx.x == 0) {
+        atomicMax(&slot->key, k);
+        __threadfence();  // the maximum is visible before this CTA counts as done
+        s_last = atomicAdd(&slot->done, 1u) == gridDim.x - 1;
     }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const unsigned long long best = atomicAdd(&slot->key, 0ull);  // every CTA's maximum is in
+    write_tokens(p, b, n, (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull)));
 }
 
 // Launch with a (kCluster, 1, 1) cluster and programmatic dependent launch.
@@ -284,7 +307,7 @@ cudaError_t launch_cluster(K kernel, dim3 grid, cudaStream_t s, const AcceptPara
 
 extern "C" size_t verify_attn_accept_workspace_bytes(int num_seqs, int T) {
     if (num_seqs < 1 || T < 1) return 0;
-    return sizeof(va::PosStats) * (size_t)num_seqs * (size_t)(T + 1);
+    return sizeof(va::PosStats) * (size_t)num_seqs * (size_t)(T + 1) + sizeof(va::SeqSlot) * (size_t)num_seqs;
 }
 
 extern "C" int verify_attn_accept(const float *target_logits, const float *draft_logits,
@@ -301,6 +324,7 @@ extern "C" int verify_attn_accept(const float *target_logits, const float *draft
     p.d = draft_tokens;
     p.tau = temperature;
     p.stats = static_cast<va::PosStats *>(workspace);
+    p.slots = reinterpret_cast<va::SeqSlot *>(p.stats + (size_t)num_seqs * (size_t)(T + 1));
     p.out = out_tokens;
     p.nacc = num_accepted;
     p.seed = seed;
@@ -309,7 +333,11 @@ extern "C" int verify_attn_accept(const float *target_logits, const float *draft
     p.V = vocab;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = va::launch_cluster(va::stats_kernel, dim3(va::kCluster, T + 1, num_seqs), s, p);
-    if (e == cudaSuccess) e = va::launch_cluster(va::decide_kernel, dim3(va::kCluster, num_seqs), s, p);
+    // a row of race CTAs per sequence, kRacePerThread vocabulary entries per thread
+    const int nrace = (int)std::min<long long>(
+        va::kMaxRaceCtas, std::max<long long>(1, ((long long)vocab + va::kRaceThreads * va::kRacePerThread - 1) /
+                                                     (va::kRaceThreads * va::kRacePerThread)));
+    if (e == cudaSuccess) e = va::launch_pdl(va::decide_kernel, dim3(nrace, num_seqs), dim3(va::kRaceThreads), 0, s, p);
     if (e != cudaSuccess) {
         va::note_cuda_error(e);
         return VA_ERR_CUDA;
