@@ -317,7 +317,7 @@ def lookup_draft_timing(va, wl, w, reps=50):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
     return {"us_per_call": us, "history_tokens": int(sum(lens)), "num_seqs": len(lens),
-            "note": "verify_attn_lookup_draft, 6..12-token match, 16 drafts, one CTA per sequence"}
+            "note": "verify_attn_lookup_draft, 6..12-token match, 16 drafts, one cluster of up to 8 CTAs per sequence"}
 
 
 def accept_timing(va, w, reps=20, vocab=151_936):

@@ -24,7 +24,7 @@ using namespace sm100;
 constexpr int kThreads = 1024;
 constexpr int kMaxMatch = 32;
 constexpr int kMaxCluster = 8;          // portable cluster size
-constexpr int kTokensPerCta = 16384;    // history slice one CTA scans, at most (sets the cluster size)
+constexpr int kTokensPerCta = 4096;     // history tokens per CTA of the cluster (up to kMaxCluster CTAs)
 
 struct DraftParams {
     const int32_t *tokens;
