@@ -151,3 +151,13 @@ def test_verify_attn_without_plan_reports_no_plan():
 
 def test_destroy_null_is_noop():
     va.library().verify_attn_plan_destroy(ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("B,T", [(1, 1), (1, 16), (64, 5), (3, 7)])
+def test_accept_workspace_size(B, T):
+    """Host only: one 32-byte statistics record per (sequence, position) plus
+    one 16-byte race slot per sequence; 0 for arguments the call rejects."""
+    lib = va.library()
+    assert lib.verify_attn_accept_workspace_bytes(B, T) == 32 * B * (T + 1) + 16 * B
+    assert lib.verify_attn_accept_workspace_bytes(0, T) == 0
+    assert lib.verify_attn_accept_workspace_bytes(B, 0) == 0
