@@ -169,10 +169,41 @@ def cpu_baseline(w, wl, min_seconds=10.0):
         dt += time.perf_counter() - t0
         n += chunk
     byts = wl.algorithmic_bytes(w) * n / len(all_rows)
+    # the same oracle on one thread (its only parallelism is the loop over
+    # rows), a shorter sample of 8-row chunks
+    n1, dt1 = 0, 0.0
+    while dt1 < min(3.0, min_seconds / 3):
+        rows = [all_rows[(n1 + k) % len(all_rows)] for k in range(8)]
+        t0 = time.perf_counter()
+        oracle.verify_attn_rows(w, rows, nthreads=1)
+        dt1 += time.perf_counter() - t0
+        n1 += 8
+    oracle.max_threads(cores)  # back to the full thread count
+    byts1 = wl.algorithmic_bytes(w) * n1 / len(all_rows)
     return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} query rows ({n / len(all_rows):.2f} x the workload's {len(all_rows)}), "
                       f"chunks of {chunk}, fp64, {dt:.1f} s",
-            "seconds": dt}
+            "seconds": dt, "cpu_model": cpu_model(),
+            "single_thread": {"value": byts1 / dt1 / 1e9, "unit": "GB/s", "sample": f"{n1} query rows, {dt1:.1f} s"}}
+
+
+def cpu_model():
+    """The host CPU's model name as the OS reports it (best effort)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model Name", "Hardware"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key and ":" in line:
+                    return line.split(":", 1)[1].strip()
+        parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                        if line.split(":")[0].strip() == "CPU part" and ":" in line})
+        if parts:
+            return f"{platform.machine()} (CPU part {', '.join(parts)})"
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
