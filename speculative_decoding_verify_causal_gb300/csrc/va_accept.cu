@@ -157,36 +157,75 @@ __device__ float cluster_sum(float v, float *slot) {
     return s;
 }
 
-// This CTA's slice [lo, hi) of a V-long row.
-__device__ __forceinline__ void slice(int V, int &lo, int &hi) {
+// This CTA's slice [lo, hi) of a V-long row; lo is a multiple of `unit`.
+__device__ __forceinline__ void slice(int V, int &lo, int &hi, int unit = 1) {
     const int r = (int)cluster_rank(), n = (int)cluster_size();
-    const int per = (V + n - 1) / n;
+    const int per = ((V + n - 1) / n + unit - 1) / unit * unit;
     lo = min(V, r * per);
     hi = min(V, lo + per);
+}
+
+constexpr int kVec = 4;  // 16-byte loads of a thread issued together in a row pass
+
+// f(i, row[i]) for every i of [lo, hi).  With a 16-byte aligned row and V a
+// multiple of 4 (then lo and hi are too): rounds of kVec unconditional
+// 16-byte loads per thread, all issued before any is used, then single
+// 16-byte loads for the rest; otherwise one entry at a time.
+template <typename F>
+__device__ __forceinline__ void row_pass(const float *row, int lo, int hi, bool vec, F f) {
+    const int step = (int)blockDim.x;
+    if (!vec) {
+        for (int i = lo + (int)threadIdx.x; i < hi; i += step) f(i, row[i]);
+        return;
+    }
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+    const int hi4 = hi >> 2;
+    int j = (lo >> 2) + (int)threadIdx.x;
+    for (; j + (kVec - 1) * step < hi4; j += kVec * step) {
+        float4 x[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) x[u] = __ldg(r4 + j + u * step);
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int i = 4 * (j + u * step);
+            f(i, x[u].x);
+            f(i + 1, x[u].y);
+            f(i + 2, x[u].z);
+            f(i + 3, x[u].w);
+        }
+    }
+    for (; j < hi4; j += step) {
+        const float4 x = __ldg(r4 + j);
+        f(4 * j, x.x);
+        f(4 * j + 1, x.y);
+        f(4 * j + 2, x.z);
+        f(4 * j + 3, x.w);
+    }
 }
 
 // Row statistics over the cluster: max (and its smallest index) of row * scale,
 // and the log-sum-exp of row * scale when want_lse.
 __device__ void row_stats(const float *row, int V, float scale, bool want_lse, unsigned long long *redk,
                           float *redf, unsigned long long *slot_k, float *slot_f, float &lse, int &argmax) {
+    const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     int lo, hi;
-    slice(V, lo, hi);
+    slice(V, lo, hi, vec ? 4 : 1);
     unsigned long long k = 0;
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-        const unsigned long long c = vkey(row[i] * scale, i);
+    row_pass(row, lo, hi, vec, [&](int i, float x) {
+        const unsigned long long c = vkey(x * scale, i);
         k = c > k ? c : k;
-    }
+    });
     k = cluster_max_u64(block_max_u64(k, redk), slot_k);
     argmax = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
     if (!want_lse) return;
     const float m = unordered((uint32_t)(k >> 32));
     float s = 0.f;
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) s += expf(row[i] * scale - m);
+    row_pass(row, lo, hi, vec, [&](int, float x) { s += expf(x * scale - m); });
     s = cluster_sum(block_sum(s, redf), slot_f);
     lse = m + logf(s);
 }
 
-__global__ void __launch_bounds__(kThreads) stats_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(kThreads, 2) stats_kernel(const AcceptParams p) {
     __shared__ unsigned long long redk[kThreads / 32];
     __shared__ float redf[kThreads / 32];
     __shared__ unsigned long long slot_k;
