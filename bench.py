@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--path", default="auto", choices=["auto", "warp", "mma"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the figures of the other named configurations")
     ap.add_argument("--soak-s", type=float, default=1.5, help="seconds of replays for the clock record")
     return ap.parse_args()
 
@@ -389,6 +391,143 @@ def accept_timing(va, w, reps=20, vocab=151_936):
     return res
 
 
+def timed_windows(replay, stream, n_windows, calls_per_window):
+    """Median and spread of the per-call time over `n_windows` back-to-back
+    windows, each one `replay()` of a graph of `calls_per_window` calls
+    bracketed by CUDA events on the launching stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_windows)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 / calls_per_window for a, b in ev)
+    return {"median_us": statistics.median(us), "min_us": us[0], "max_us": us[-1], "windows": n_windows,
+            "calls_per_window": calls_per_window}
+
+
+class ConfigRun:
+    """One named configuration on the device: its plan, enough cache copies
+    that consecutive calls read their KV from HBM, and CUDA graphs of one
+    rotation of calls (plain, and with an event pair around every
+    partial-attention kernel)."""
+
+    def __init__(self, va, wl, name, dev, stream, path="auto"):
+        import torch
+        self.va, self.wl, self.name, self.stream = va, wl, name, stream
+        self.w = w = wl.config_workload(name)
+        self.nbytes = wl.algorithmic_bytes(w)
+        self.kv_bytes = self.nbytes - 2 * w["q"].size * 2
+        self.copies = 1 if self.kv_bytes > 4 * L2_BYTES else int(math.ceil(4 * L2_BYTES / self.kv_bytes))
+        self.d = d = wl.to_device(w, dev, copies=self.copies)
+        self.plan_times = []
+        for _ in range(5):
+            t0 = time.perf_counter()
+            p = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=path)
+            self.plan_times.append((time.perf_counter() - t0) * 1e6)
+            p.destroy()
+        self.plan = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=path)
+        self.info = self.plan.info()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                self.call(i, stream)
+        torch.cuda.synchronize()
+        self.ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                         for _ in range(self.copies)]
+        for a, b in self.ev_pairs:  # torch creates the CUDA event on first record
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        self.g_full = self.capture(self.copies, False)
+        self.g_events = self.capture(self.copies, True)
+
+    def call(self, i, s, cache=None):
+        w, d = self.w, self.d
+        k, v, ks, vs = d["caches"][(i if cache is None else cache) % self.copies]
+        self.va.verify_attn_with_plan(self.plan, d["q"], k, v, ks, vs, d["block_table"], d["seq_lens"], w["T"],
+                                      d["out"], d["lse"], stream=s)
+
+    def capture(self, n, with_events, cache=None):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            s = torch.cuda.current_stream()
+            for i in range(n):
+                if with_events:
+                    self.va.verify_attn_plan_set_events(self.plan, *self.ev_pairs[i])
+                self.call(i, s, cache)
+            self.va.verify_attn_plan_set_events(self.plan, None, None)
+        return g
+
+    def calls_per_replay(self, min_calls):
+        return self.copies * max(1, int(math.ceil(min_calls / self.copies)))
+
+    def window_timing(self, n_windows=7, min_calls=40):
+        reps = max(1, int(math.ceil(min_calls / self.copies)))
+
+        def replay():
+            for _ in range(reps):
+                self.g_full.replay()
+        with torch_stream(self.stream):
+            replay()  # warm
+        return timed_windows(replay, self.stream, n_windows, reps * self.copies)
+
+    def partial_kernel_us(self, reps=3):
+        """Mean CUDA-event time of the partial-attention kernel alone (events
+        recorded on the launching stream around it, inside a graph)."""
+        import torch
+        vals = []
+        with torch.cuda.stream(self.stream):
+            for _ in range(reps):
+                self.g_events.replay()
+                torch.cuda.synchronize()
+                vals.extend(a.elapsed_time(b) * 1e3 for a, b in self.ev_pairs)
+        return statistics.median(vals)
+
+    def hot_l2_us(self):
+        """Same cache copy every call (stays in L2 when it fits): labelled, not the headline."""
+        g = self.capture(self.copies, False, cache=0)
+        return timed_windows(lambda: g.replay(), self.stream, 5, self.copies)["median_us"]
+
+    def close(self):
+        self.plan.destroy()
+
+
+class torch_stream:
+    def __init__(self, s):
+        import torch
+        self.ctx = torch.cuda.stream(s)
+
+    def __enter__(self):
+        return self.ctx.__enter__()
+
+    def __exit__(self, *a):
+        return self.ctx.__exit__(*a)
+
+
+def config_record(run, peak, launch_bound_bytes=8e6):
+    """Per-configuration figures: median / spread of the call over several
+    windows, and (where the event pair around the partial kernel brackets it
+    tighter than the call) the partial kernel's own time and roofline
+    fraction.  Launch-bound configurations report microseconds per call only."""
+    win = run.window_timing()
+    rec = {"workload": run.wl.CONFIGS[run.name].description, "algorithmic_bytes": run.nbytes,
+           "us_per_call": win["median_us"], "us_per_call_min": win["min_us"], "us_per_call_max": win["max_us"],
+           "windows": win["windows"], "calls_per_window": win["calls_per_window"],
+           "GB/s": run.nbytes / (win["median_us"] * 1e-6) / 1e9,
+           "frac_of_peak_hbm": run.nbytes / (win["median_us"] * 1e-6) / 1e9 / peak,
+           "num_items": run.info["num_items"], "max_splits": run.info["max_splits"], "path": run.info["path"]}
+    k_us = run.partial_kernel_us()
+    if run.nbytes >= launch_bound_bytes and k_us < win["median_us"]:
+        rec["kernel_us"] = k_us
+        rec["kernel_frac_of_peak_hbm"] = run.nbytes / (k_us * 1e-6) / 1e9 / peak
+    else:
+        rec["note"] = "launch-bound: microseconds per call only (event bracketing of the kernel is not meaningful here)"
+    return rec
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -403,61 +542,21 @@ def run_ours(args):
     import speculative_decoding_verify_causal_gb300 as va
     from speculative_decoding_verify_causal_gb300 import workloads as wl
 
-    w = wl.config_workload(args.config)
-    nbytes = wl.algorithmic_bytes(w)
-    kv_bytes = nbytes - 2 * w["q"].size * 2
-    copies = 1 if kv_bytes > 4 * L2_BYTES else int(math.ceil(4 * L2_BYTES / kv_bytes))
-    d = wl.to_device(w, dev, copies=copies)
     stream = torch.cuda.Stream(dev)
-
-    # plan (host) cost, then the plan used by the timed loop
-    plan_times = []
-    for _ in range(5):
-        t0 = time.perf_counter()
-        p = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=args.path)
-        plan_times.append((time.perf_counter() - t0) * 1e6)
-        p.destroy()
-    plan = va.verify_attn_plan(w["seq_lens"], w["T"], w["Hq"], w["Hkv"], w["D"], w["kv_dtype"], path=args.path)
-    info = plan.info()
+    peak, peak_src = peaks()
+    run = ConfigRun(va, wl, args.config, dev, stream, path=args.path)
+    w, d, plan, info, nbytes, copies = run.w, run.d, run.plan, run.info, run.nbytes, run.copies
     launches_per_step = 1 + (1 if info["num_split_groups"] > 0 else 0)
 
-    def call(i, s):
-        k, v, ks, vs = d["caches"][i % copies]
-        va.verify_attn_with_plan(plan, d["q"], k, v, ks, vs, d["block_table"], d["seq_lens"], w["T"],
-                                 d["out"], d["lse"], stream=s)
-
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            call(i, stream)
-    torch.cuda.synchronize()
-
-    # capture one graph of `copies` calls (and one for the remainder), with an
-    # event pair around every partial-attention kernel
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(copies)]
-    for a, b in ev_pairs:  # torch creates the CUDA event on first record
-        a.record(stream)
-        b.record(stream)
-    torch.cuda.synchronize()
-
-    def capture(n, with_events):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            s = torch.cuda.current_stream()
-            for i in range(n):
-                if with_events:
-                    va.verify_attn_plan_set_events(plan, *ev_pairs[i])
-                call(i, s)
-            va.verify_attn_plan_set_events(plan, None, None)
-        return g
-
-    # the timed graph carries no event nodes; a second copy with an event
-    # pair around every partial-attention kernel gives that kernel's time
-    g_full = capture(copies, False)
-    g_events = capture(copies, True)
+    # the contract's timed region: exactly args.steps calls (whole rotations
+    # from the graph, the remainder from a second graph)
     rem = args.steps % copies
-    g_rem = capture(rem, False) if rem else None
+    g_rem = run.capture(rem, False) if rem else None
     replays = args.steps // copies
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // copies)):
+            run.g_full.replay()
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -470,7 +569,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(replays):
-            g_full.replay()
+            run.g_full.replay()
         if g_rem is not None:
             g_rem.replay()
         t_end.record(stream)
@@ -478,45 +577,21 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    partial_ms = None
-    try:
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g_events.replay()
-        torch.cuda.synchronize()
-        partial_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs)
-    except Exception:
-        partial_ms = None
-    # hot-L2 figure (labelled as such, not the metric): every call reads the
-    # same cache copy, which stays in L2 when it fits
-    hot = None
-    if kv_bytes < L2_BYTES:
-        g_hot = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_hot, stream=stream):
-            s = torch.cuda.current_stream()
-            for _ in range(copies):
-                call(0, s)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g_hot.replay()
-            h0 = torch.cuda.Event(enable_timing=True)
-            h1 = torch.cuda.Event(enable_timing=True)
-            h0.record(stream)
-            for _ in range(10):
-                g_hot.replay()
-            h1.record(stream)
-        torch.cuda.synchronize()
-        hot_ms = h0.elapsed_time(h1) / (10 * copies)
-        hot = {"us_per_call": hot_ms * 1e3, "value": world * nbytes / (hot_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "note": "K/V served from L2 (same cache copy every call); not the headline"}
     # keep the GPU busy with the same graph so the clock record sees the load
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         while time.perf_counter() - t0 < args.soak_s:
             for _ in range(50):
-                g_full.replay()
+                run.g_full.replay()
             torch.cuda.synchronize()
     clocks = sampler.stop()
+    head = config_record(run, peak)
+    partial_us = head.get("kernel_us")
+    hot = None
+    if run.kv_bytes < L2_BYTES:
+        hot_us = run.hot_l2_us()
+        hot = {"us_per_call": hot_us, "value": world * nbytes / (hot_us * 1e-6) / 1e9, "unit": "GB/s",
+               "note": "K/V served from L2 (same cache copy every call); not the headline"}
 
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -561,25 +636,40 @@ def run_ours(args):
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
         e2e = {"value": whole_job_rate(nbytes, 1, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "us_per_call": e2e_ms * 1e3, "steps": n_e2e}
+        del host, dev_in
 
     append = kv_append_timing(va, w, d, stream)
     lookup = lookup_draft_timing(va, wl, w)
     acc = accept_timing(va, w)
+    plan_us = statistics.median(run.plan_times)
+    run.close()
+
+    # every other named configuration, one after the other (figures only; the
+    # headline above is args.config)
+    per_config = {args.config: head}
+    if not args.no_per_config and world == 1:
+        del d
+        for name in ("tiny", "mtp4", "batched", "maxctx", "lookup16"):
+            if name == args.config:
+                continue
+            torch.cuda.empty_cache()
+            r = ConfigRun(va, wl, name, dev, stream, path=args.path)
+            per_config[name] = config_record(r, peak)
+            r.close()
+            del r
 
     if rank != 0:
-        plan.destroy()
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
 
-    peak, peak_src = peaks()
     kernel = "va_mma_partial" if info["path"] == 2 else "va_warp_partial"
     roof = None
-    if partial_ms:
-        achieved = nbytes / (partial_ms * 1e-3) / 1e9
+    if partial_us:
+        achieved = nbytes / (partial_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic_record(kernel, args.config), "kernel": kernel,
-                "kernel_us": partial_ms * 1e3, "peak_source": peak_src,
+                "kernel_us": partial_us, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": nbytes}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -595,12 +685,13 @@ def run_ours(args):
             "kv_dtype": w["kv_dtype"], "T": w["T"], "seq_lens_sum": int(w["seq_lens"].sum()),
             "num_seqs": int(len(w["seq_lens"])), "Hq": w["Hq"], "Hkv": w["Hkv"], "head_dim": w["D"],
             "algorithmic_bytes": nbytes,
-            "l2": (f"rotating {copies} cache copies ({copies * kv_bytes / 1e6:.0f} MB >= 4x L2)"
+            "l2": (f"rotating {copies} cache copies ({copies * run.kv_bytes / 1e6:.0f} MB >= 4x L2)"
                    if copies > 1 else "cache larger than 4x L2"),
             "graph": "CUDA graph replay", "parallelism": f"replicas x{world}",
-            "plan": info, "plan_us": statistics.median(plan_times),
+            "plan": info, "plan_us": plan_us,
         },
         "roofline": roof,
+        "per_config": per_config,
         "hot_l2": hot,
         "kv_append": append,
         "lookup_draft": lookup,
@@ -611,7 +702,6 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
     }
     print(json.dumps(line), flush=True)
-    plan.destroy()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0

@@ -175,9 +175,14 @@ int verify_attn_plan_describe(const int32_t *seq_lens_host, int num_seqs, int T,
                               const va_plan_options *opts, va_plan_info *info,
                               int32_t *items, int max_items);
 
-/* Read (and if clear != 0, reset) the plan's device flag word: bit 0 = a
- * block-table entry outside [0, num_pages) was skipped, bit 1 = a device
- * seq_lens value differed from the planned one.  Synchronises the stream. */
+/* Read (and if clear != 0, reset) the plan's device flag word:
+ *   bit 0 (1) = a block-table entry outside [0, num_pages) was skipped;
+ *   bit 1 (2) = a device seq_lens value differed from the planned one;
+ *   bit 2 (4) = a wait inside the tensor-core kernel's pipeline gave up after
+ *               its time limit (2 s); the CTA stopped early and its rows of
+ *               out / lse are not valid.  It means a hardware or scheduling
+ *               fault, never a property of the inputs.
+ * Synchronises the stream. */
 int verify_attn_plan_device_flags(const va_plan *plan, int clear, int *flags,
                                   void *stream);
 
@@ -211,27 +216,41 @@ const char *verify_attn_last_cuda_error_string(void);
  * keeps the work list and the split partials in a static device array of
  * VA_NOALLOC_SCRATCH_BYTES instead of a plan's workspace.  The caller passes
  * every input and output exactly as for verify_attn (same layouts), plus the
- * block-table row stride (0 = max_b ceil(L_b / 16)).  When the partials of
- * the default split do not fit, the split is made coarser until they do; a
- * problem whose work list alone does not fit returns
- * VA_ERR_SCRATCH_TOO_SMALL.  Nothing is allocated: no cudaMalloc, no
- * cudaFree, no allocating library call.
+ * block-table row stride (0 = max_b ceil(L_b / 16)) and the page-pool size
+ * num_pages (> 0: every block-table entry is checked against [0, num_pages),
+ * a bad one is skipped and flagged as with a plan; 0: unchecked).  When the
+ * partials of the default split do not fit, the split is made coarser until
+ * they do; a problem whose work list alone does not fit returns
+ * VA_ERR_SCRATCH_TOO_SMALL before anything touches the device.  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * It always runs the CUDA-core partial kernel (the one a plan picks below 16
+ * packed rows), also where a plan would pick the tensor-core kernel, so at
+ * long contexts with many packed rows it is several times slower than
+ * verify_attn_with_plan.
  *
  * The first call on a device looks up the array's device address there
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array, and each call
- * overwrites what the previous one left there (its flag word is cleared at
- * the start of every call): calls that overlap on the GPU race, so order them
- * on one stream.  Asynchronous like verify_attn; the host-to-device copy of
- * the work list is made from pageable host memory. */
+ * (cudaGetSymbolAddress, with that device current).  All calls share the one
+ * array, and each call overwrites what the previous one left there (its flag
+ * word is cleared at the start of every call): calls that overlap on the GPU
+ * race, so order them on one stream.  The work list is copied from static,
+ * pageable host buffers with cudaMemcpyAsync on every call, so a call must
+ * not be captured into a CUDA graph (a replay would not see later work
+ * lists).  Asynchronous like verify_attn. */
 int verify_attn_noalloc(const int32_t *seq_lens_host, int num_seqs, int T,
                         int num_q_heads, int num_kv_heads, int head_dim,
                         va_kv_dtype kv_dtype, const void *q,
                         const void *k_pages, const void *v_pages,
                         const float *k_scale, const float *v_scale,
                         const int32_t *block_table, int block_table_stride,
-                        const int32_t *seq_lens, void *out, float *lse,
-                        void *stream);
+                        int num_pages, const int32_t *seq_lens, void *out,
+                        float *lse, void *stream);
+
+/* The flag word that the most recent verify_attn_noalloc call on the current
+ * device left in the static scratch (same bits as
+ * verify_attn_plan_device_flags); clear != 0 resets it.  Synchronises the
+ * stream. */
+int verify_attn_noalloc_flags(int clear, int *flags, void *stream);
 
 /* KV append with quantise-on-write: the step just before verify attention.
  * The verify forward computes K and V for its T tokens and stores them in the

@@ -96,7 +96,9 @@ def _load():
         lib.verify_attn_last_cuda_error.restype = I
         lib.verify_attn_last_cuda_error_string.argtypes = []
         lib.verify_attn_last_cuda_error_string.restype = ctypes.c_char_p
-        lib.verify_attn_noalloc.argtypes = [P, I, I, I, I, I, I] + [P] * 6 + [I, P, P, P, P]
+        lib.verify_attn_noalloc.argtypes = [P, I, I, I, I, I, I] + [P] * 6 + [I, I, P, P, P, P]
+        lib.verify_attn_noalloc_flags.argtypes = [I, ctypes.POINTER(I), P]
+        lib.verify_attn_noalloc_flags.restype = I
         lib.verify_attn_noalloc.restype = I
         lib.verify_attn_kv_append.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, I, P, I, P, P]
         lib.verify_attn_kv_append.restype = I
@@ -314,20 +316,33 @@ def verify_attn_plan_set_events(plan: Plan, ev_before=None, ev_after=None):
 
 def verify_attn_noalloc(seq_lens_host, T, num_q_heads, num_kv_heads, head_dim, kv_dtype, q, k_pages,
                         v_pages, k_scale, v_scale, block_table, seq_lens, out, lse=None,
-                        block_table_stride=0, stream=None):
+                        block_table_stride=0, num_pages=0, stream=None):
     """Verify attention that allocates no device memory: plans from the host
     ``seq_lens_host`` on every call and keeps its scratch in the library's
     static device array (see ``include/verify_attn.h``).  For callers that
     cannot call cudaMalloc.  Calls share that array, so order them on one
-    stream; make the first call on a device before any stream capture."""
+    stream; not for CUDA-graph capture.  ``num_pages`` > 0 checks every
+    block-table entry (bad ones are skipped and flagged, see
+    ``verify_attn_noalloc_flags``)."""
     lens = _host_lens(seq_lens_host)
     code = _dtype_code(kv_dtype)
     args, tail, s = _marshal(code, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
                              stream)
     rc = _load().verify_attn_noalloc(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T), int(num_q_heads),
                                      int(num_kv_heads), int(head_dim), code, *args[:6],
-                                     int(block_table_stride), args[6], *tail, s)
+                                     int(block_table_stride), int(num_pages), args[6], *tail, s)
     _check(rc, "verify_attn_noalloc")
+
+
+def verify_attn_noalloc_flags(clear=True, stream=None):
+    """Flag word of the last verify_attn_noalloc call on the current device
+    (same bits as verify_attn_plan_device_flags); clears it by default."""
+    import torch
+    stream = stream or torch.cuda.current_stream()
+    flags = ctypes.c_int(0)
+    _check(_load().verify_attn_noalloc_flags(int(bool(clear)), ctypes.byref(flags),
+                                             ctypes.c_void_p(stream.cuda_stream)), "verify_attn_noalloc_flags")
+    return flags.value
 
 
 def verify_attn_kv_append(k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, T,
@@ -430,6 +445,7 @@ __all__ = [
     "verify_attn_lookup_draft",
     "verify_attn_kv_append",
     "verify_attn_noalloc",
+    "verify_attn_noalloc_flags",
     "verify_attn_plan_set_events",
     "verify_attn_plan", "verify_attn", "verify_attn_with_plan", "verify_attn_plan_destroy",
     "verify_attn_status_string", "verify_attn_plan_get_info", "verify_attn_plan_describe",

@@ -12,7 +12,11 @@
 // memory: its device address is fetched once per device with
 // cudaGetSymbolAddress (that device current) and passed to the kernels.
 // Every call shares the array and overwrites the previous call's contents;
-// the flag word is cleared at the start of each call.
+// the flag word is cleared at the start of each call and can be read back
+// with verify_attn_noalloc_flags.  The work list is staged in static host
+// buffers and copied with cudaMemcpyAsync from pageable memory, so a call is
+// not meant to be captured into a CUDA graph.  Only the CUDA-core partial
+// kernel runs here (for every packed-row count).
 #include <cmath>
 #include <mutex>
 
@@ -42,7 +46,9 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // count, looked up once with the device current.
 int device_setup(void **scratch, int *num_sms) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        va::note_cuda_error(e);
         cudaGetLastError();
         return VA_ERR_NO_DEVICE;
     }
@@ -50,12 +56,16 @@ int device_setup(void **scratch, int *num_sms) {
     std::lock_guard<std::mutex> lk(g_setup_mu);
     if (!g_scratch_dev[dev]) {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) {
+            va::note_cuda_error(e);
             cudaGetLastError();
             return VA_ERR_CUDA;
         }
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || n < 1) {
+            va::note_cuda_error(e);
             cudaGetLastError();
             return VA_ERR_NO_DEVICE;
         }
@@ -102,14 +112,22 @@ bool layout_for(const int32_t *lens, int B, int Hkv, int D, int split, Layout &L
     return true;
 }
 
+// A failing CUDA call: remember it for verify_attn_last_cuda_error and
+// reset the runtime's last-error state.
+int cuda_fail(cudaError_t e) {
+    va::note_cuda_error(e);
+    cudaGetLastError();
+    return VA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, int Hq, int Hkv,
                                    int D, va_kv_dtype kv_dtype, const void *q, const void *k_pages,
                                    const void *v_pages, const float *k_scale,
                                    const float *v_scale, const int32_t *block_table,
-                                   int block_table_stride, const int32_t *seq_lens, void *out,
-                                   float *lse, void *stream) {
+                                   int block_table_stride, int num_pages, const int32_t *seq_lens,
+                                   void *out, float *lse, void *stream) {
     if (!seq_lens_host || B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv)
         return VA_ERR_INVALID_ARGUMENT;
     if (D != 64 && D != 128 && D != 256) return VA_ERR_UNSUPPORTED;
@@ -127,24 +145,27 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
         total_len += seq_lens_host[b];
         max_len = seq_lens_host[b] > max_len ? seq_lens_host[b] : max_len;
     }
-    if (block_table_stride < 0 || (block_table_stride > 0 && block_table_stride < max_pages))
+    if (block_table_stride < 0 || (block_table_stride > 0 && block_table_stride < max_pages) || num_pages < 0)
         return VA_ERR_INVALID_ARGUMENT;
     const int bt_stride = block_table_stride > 0 ? block_table_stride : max_pages;
 
-    void *scratch = nullptr;
-    int num_sms = 0;
-    int rc = device_setup(&scratch, &num_sms);
-    if (rc != VA_OK) return rc;
-
     // Geometry: the CUDA-core kernel's row groups and key tile, one wave of
     // splits over the SMs (2 resident CTAs each), made coarser until the
-    // split partials fit in the scratch.
+    // split partials fit in the scratch.  A problem that does not fit even
+    // unsplit is rejected here, before any CUDA call.
     const int G = Hq / Hkv;
     const int R = G * T;
     Layout L{};
     L.num_row_groups = (R + va::kWarpRows - 1) / va::kWarpRows;
     L.rows_per_group = (R + L.num_row_groups - 1) / L.num_row_groups;
     L.tile = va::kWarpTile;
+    if (!layout_for(seq_lens_host, B, Hkv, D, max_len, L) || L.total > VA_NOALLOC_SCRATCH_BYTES)
+        return VA_ERR_SCRATCH_TOO_SMALL;
+
+    void *scratch = nullptr;
+    int num_sms = 0;
+    int rc = device_setup(&scratch, &num_sms);
+    if (rc != VA_OK) return rc;
     const long long slots = 2LL * num_sms;
     long long c = (total_len + slots - 1) / slots;
     c = (c + L.tile - 1) / L.tile * L.tile;
@@ -183,14 +204,12 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
             }
     }
     // Pageable sources: each copy has read the host buffer when it returns.
-    if (cudaMemsetAsync(base, 0, kFlagsBytes, s) != cudaSuccess ||
-        cudaMemcpyAsync(base + L.off_items, g_host_items, sizeof(va::Item) * ni,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        (ng > 0 && cudaMemcpyAsync(base + L.off_groups, g_host_groups, sizeof(va::Group) * ng,
-                                   cudaMemcpyHostToDevice, s) != cudaSuccess)) {
-        cudaGetLastError();
-        return VA_ERR_CUDA;
-    }
+    cudaError_t e = cudaMemsetAsync(base, 0, kFlagsBytes, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(base + L.off_items, g_host_items, sizeof(va::Item) * ni, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && ng > 0)
+        e = cudaMemcpyAsync(base + L.off_groups, g_host_groups, sizeof(va::Group) * ng, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
 
     va::PartialParams pp{};
     pp.q = static_cast<const uint16_t *>(q);
@@ -213,10 +232,11 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     pp.G = G;
     pp.R = R;
     pp.rows_per_group = L.rows_per_group;
-    pp.num_pages = 0;
+    pp.num_pages = num_pages;  // 0: block-table entries unchecked
     pp.num_parts = L.num_parts;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-    if (va::launch_warp_partial(pp, D, kv_dtype, ni, s) != cudaSuccess) return VA_ERR_CUDA;
+    e = va::launch_warp_partial(pp, D, kv_dtype, ni, s);
+    if (e != cudaSuccess) return cuda_fail(e);
     if (ng > 0) {
         va::CombineParams cp{};
         cp.groups = reinterpret_cast<const va::Group *>(base + L.off_groups);
@@ -230,7 +250,24 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
         cp.R = R;
         cp.rows_per_group = L.rows_per_group;
         cp.D = D;
-        if (va::launch_combine(cp, ng, L.max_splits, s) != cudaSuccess) return VA_ERR_CUDA;
+        e = va::launch_combine(cp, ng, L.max_splits, s);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
+    return VA_OK;
+}
+
+extern "C" int verify_attn_noalloc_flags(int clear, int *flags, void *stream) {
+    if (!flags) return VA_ERR_INVALID_ARGUMENT;
+    void *scratch = nullptr;
+    int num_sms = 0;
+    int rc = device_setup(&scratch, &num_sms);
+    if (rc != VA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, scratch, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(scratch, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *flags = host;
     return VA_OK;
 }

@@ -108,12 +108,15 @@ def _normal_rows(rng, n_tokens, Hkv, D):
 
 
 def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peaks=0.0,
-                  extra_pages=0, bt_stride=None, name="custom"):
+                  extra_pages=0, bt_stride=None, name="custom", k_std=1.0, v_std=1.0):
     """Build one synthetic verify-attention problem.
 
     ``seq_lens`` are the full lengths L_b (they include the T verify tokens).
     ``needles``: None, or a callable ``(rng, b, L) -> list of token positions``
-    at which every kv head gets a needle key.  Returns a dict of host arrays.
+    at which every kv head gets a needle key.  ``k_std`` / ``v_std`` scale the
+    N(0, 1) key / value rows before rounding and quantisation (1 leaves the
+    stream of the named configurations unchanged).  Returns a dict of host
+    arrays.
     """
     seq_lens = [int(x) for x in seq_lens]
     B = len(seq_lens)
@@ -145,8 +148,14 @@ def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peak
     k_flat = k_pages.reshape(num_pages * PAGE, Hkv, D)
     v_flat = v_pages.reshape(num_pages * PAGE, Hkv, D)
     for b, L in enumerate(seq_lens):
-        k = _bf16_round(_normal_rows(rng, L, Hkv, D))
-        v = _bf16_round(_normal_rows(rng, L, Hkv, D))
+        k = _normal_rows(rng, L, Hkv, D)
+        v = _normal_rows(rng, L, Hkv, D)
+        if k_std != 1.0:
+            k *= np.float32(k_std)
+        if v_std != 1.0:
+            v *= np.float32(v_std)
+        k = _bf16_round(k)
+        v = _bf16_round(v)
         pos = []
         if needles is not None:
             pos = list(needles(rng, b, L))
@@ -187,6 +196,8 @@ def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peak
         "kv_dtype": kv_dtype,
         "num_pages": num_pages,
         "needle_pos": needle_pos,
+        "k_std": float(k_std),
+        "v_std": float(v_std),
     }
 
 
