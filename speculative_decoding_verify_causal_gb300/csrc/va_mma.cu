@@ -8,9 +8,9 @@
 // idea in "Four Tesla V100s from 2017 matched my RTX 5090 on single-request
 // Qwen 3.8 decode", section "What I actually built" (lay the verify rows onto
 // the tensor instruction's row tile so the extra drafted tokens ride along
-// almost for free); keeping the cache 1 byte per element until the last step
-// before the tensor core is the same section's "keep it compressed while it is
-// read from HBM".
+// almost for free); the same section's advice to leave the data compressed
+// until the step before the tensor core is followed here: the cache stays 8-bit
+// from HBM into shared memory and is expanded right before the MMA.
 //
 // Per 64-key tile (4 pages):
 //   producer warp    stages the item's page ids, then TMA-gathers the pages
@@ -34,9 +34,13 @@
 //                    per-key k scale and the bottom-right causal mask, keep the
 //                    running max / sum (base 2; the max is only moved, and O
 //                    rescaled, when it grows by more than 2^8), write
-//                    P * v_scale (fp16) back over S in TMEM, and at the end
-//                    write O / l and the log-sum-exp (split partials leave by
-//                    TMA box stores).
+//                    P * v_scale * 2^beta (fp16) back over S in TMEM, and at
+//                    the end write O / (l 2^beta) and the log-sum-exp (split
+//                    partials leave by TMA box stores).  2^beta is a power of
+//                    two chosen from each tile's largest v scale (kept while it
+//                    still fits), so that P * v_scale stays in fp16's normal
+//                    range for value rows of any magnitude; it is folded into
+//                    the exponent, so it costs no multiply.
 // Scales are constant along head_dim, so dequantisation is an exact cast
 // and the scales are folded into the scores (k) and into P (v).
 //
@@ -66,6 +70,7 @@ constexpr int kBfStages = 3;        // bf16: 64-key stages TMA'd straight into M
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kScaleRing = 4;       // per-tile k/v scales handed to the softmax warps
+constexpr int kRingFloats = 2 * kTile + 4;  // one ring slot: k[64], v[64], largest v scale of each half, pad
 constexpr int kMaxItemPages = kMmaMaxItemTokens / VA_PAGE_SIZE;  // page ids staged in smem
 constexpr int kSetupBar = 10;       // named barrier: set-up done (producer arrives, the rest wait)
 
@@ -109,7 +114,7 @@ struct Smem {
     uint32_t conv_k, conv_v;         // kNumBuf buffers each
     uint32_t raw, raw_stride;        // raw stages
     uint32_t pids;                   // the item's page ids (kMaxItemPages ints)
-    uint32_t scale_ring;             // kScaleRing x (64 k + 64 v) floats
+    uint32_t scale_ring;             // kScaleRing slots of kRingFloats
     uint32_t xchg;                   // softmax pair exchange: [2][2][128] maxima + [2][128] sums
     uint32_t bars;                   // mbarriers
     uint32_t total;
@@ -121,7 +126,7 @@ struct Smem {
         raw_stride = C::kQuant ? C::kRawTileBytes : 0;
         pids = raw + (C::kQuant ? nst * raw_stride : 0);
         scale_ring = pids + kMaxItemPages * 4;
-        xchg = scale_ring + (C::kQuant ? kScaleRing * 2 * kTile * 4 : 0);
+        xchg = scale_ring + (C::kQuant ? kScaleRing * kRingFloats * 4 : 0);
         bars = xchg + 6 * 128 * 4;
         total = bars + 64 * 8 + 16;
     }
@@ -561,6 +566,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         const uint32_t xsum = xmax + 2 * 2 * 128 * 4;          // [half][128]
         const float c_r = p.sm_scale_log2 / q_prescale;  // score scale in log2 units
         float m_run = -INFINITY, l_run = 0.f;
+        int beta = 0;  // value normaliser of the tiles so far (quantised caches): 2^beta
         const int last_visible = it.L - T + t_r;  // bottom-right causal mask
         const uint32_t ring = sbase + L.scale_ring;  // shared address of the scale ring
         for (int i = 0; i < ntiles; ++i) {
@@ -575,7 +581,8 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 uint32_t s[32];
                 tmem_ld32(lane_tm + C::kSCol + b * kTile + half * 32, s);
                 tmem_wait_ld();
-                const uint32_t ks = ring + (i % kScaleRing) * 2 * kTile * 4 + half * 32 * 4;
+                const uint32_t slot = ring + (i % kScaleRing) * kRingFloats * 4;
+                const uint32_t ks = slot + half * 32 * 4;
                 const uint32_t vs = ks + kTile * 4;
                 // pages outside the pool (only checked when the pool size is
                 // known) were replaced by page 0 when loading: mask their keys
@@ -641,7 +648,30 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                     m_run = m_tile;
                     l_run *= alpha;
                 }
-                if (__any_sync(0xffffffffu, rescale) && i > 0) {
+                // Value normaliser (quantised caches): P carries p * v_scale * 2^beta
+                // with 2^beta bringing the tile's largest v scale into [1, 2); beta
+                // is kept while that product stays in [2^-6, 4), so that P stays in
+                // fp16's normal range whatever the values' magnitude.  Every thread
+                // takes the same decision from the same two maxima; O, which holds
+                // the earlier tiles at the previous beta, follows a change.
+                int dbeta = 0;
+                if (C::kQuant) {
+                    const float mv = fmaxf(lds_f32(slot + 4u * (2 * kTile)), lds_f32(slot + 4u * (2 * kTile + 1)));
+                    if (mv > 0.f) {
+                        const float rr = mv * __uint_as_float((uint32_t)(127 + beta) << 23);
+                        if (i == 0 || !(rr >= 0x1p-6f && rr < 4.f)) {
+                            // mv in [2^(E-127), 2^(E-126)): beta = 127 - E, capped at 118
+                            // so that p 2^beta (p <= 2^8) stays finite in fp32
+                            const int E = max(9, min(253, (int)((__float_as_uint(mv) >> 23) & 0xFFu)));
+                            dbeta = i == 0 ? 0 : (127 - E) - beta;
+                            beta = 127 - E;
+                        }
+                    }
+                }
+                // powers of two: exact
+                const float fo =
+                    dbeta == 0 ? alpha : alpha * __uint_as_float((uint32_t)(127 + max(-126, min(127, dbeta))) << 23);
+                if (__any_sync(0xffffffffu, fo != 1.f) && i > 0) {
                     // O holds the earlier tiles: wait until PV(i-1) has landed
                     // (its commit completes the ((i-1)/2)-th phase of P buffer (i-1)%2)
                     if (!mbar_wait(bar(kPEmpty + ((i - 1) & 1)), ((i - 1) >> 1) & 1, kWaitNs)) { ok = false; }
@@ -652,14 +682,14 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                         tmem_ld32(lane_tm + C::kOCol + c0, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * fo);
                         tmem_st32(lane_tm + C::kOCol + c0, o);
                     }
                     tmem_wait_st();
                 }
                 // p = 2^(x*c - m); masked keys give 2^-inf = 0 and carry a zero
                 // v scale, so no select is needed
-                const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+                const float neg_m = (m_run == -INFINITY ? 0.f : -m_run) + (float)beta;
                 const uint64_t c2 = f2_pack(__float_as_uint(c_r), __float_as_uint(c_r));
                 const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
                 uint32_t pk[16];
@@ -688,7 +718,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 }
                 uint32_t l0, l1;
                 f2_unpack(f2_add(ls[0], ls[1]), l0, l1);
-                l_run += __uint_as_float(l0) + __uint_as_float(l1);
+                l_run += (__uint_as_float(l0) + __uint_as_float(l1)) * __uint_as_float((uint32_t)(127 - beta) << 23);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kRingFree + i % kScaleRing));  // scale slot read
                 // P row r, keys [32 half, 32 half + 32) -> columns [16 half, 16 half + 16)
@@ -736,7 +766,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             sts_f32(xsum + 4u * (half * 128 + r), l_run);
             named_bar_sync(pair_bar, 64);
             const float l_tot = l_run + lds_f32(xsum + 4u * ((1 - half) * 128 + r));
-            inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            inv = l_tot > 0.f ? (1.f / l_tot) * __uint_as_float((uint32_t)(127 - beta) << 23) : 0.f;
             const float lse_nat = l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
             if (row_ok && half == 0 && ok) {  // the row's log-sum-exp
                 const int rr = row0 + r;
@@ -910,7 +940,13 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
             if (kv == 0) {  // the tile's k and v scales (zero past the end) -> ring
                 // slot i % kScaleRing held tile i - kScaleRing, whose softmax has to have read it
                 if (!mbar_wait(bar(kRingFree + i % kScaleRing), ((i / kScaleRing) & 1) ^ 1, kWaitNs)) ok = false;
-                sts_f32(ring + (i % kScaleRing) * 2 * kTile * 4 + 4u * dt, scale_out);
+                const uint32_t slot = ring + (i % kScaleRing) * kRingFloats * 4;
+                sts_f32(slot + 4u * dt, scale_out);
+                if (dt >= kTile) {  // the largest v scale of this warp's 32 keys (scales are >= 0:
+                                    // their bits order like unsigned integers)
+                    const uint32_t mv = __reduce_max_sync(0xffffffffu, __float_as_uint(scale_out));
+                    if (lane == 0) sts_u32(slot + 4u * (2 * kTile + (dt - kTile) / 32), mv);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
