@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "int8": 2}
+KV_DTYPES = {"bf16": 0, "fp8_e4m3": 1, "int8": 2, "int4": 3, "int2": 4}
 
 
 def build(force: bool = False) -> str:
@@ -56,6 +56,8 @@ def _load():
         lib.oracle_verify_attn_partial.restype = I
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_decode_packed.argtypes = [P, ctypes.c_size_t, I]
+        lib.oracle_decode_packed.restype = ctypes.c_double
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_max_threads.argtypes = [I]
@@ -83,7 +85,7 @@ def _c(a, dtype):
 def _common(w):
     """Argument tuple shared by every entry point, from a workload dict."""
     dt = w["kv_dtype"]
-    raw = np.uint16 if dt == "bf16" else (np.uint8 if dt == "fp8_e4m3" else np.int8)
+    raw = {"bf16": np.uint16, "fp8_e4m3": np.uint8, "int8": np.int8, "int4": np.uint8, "int2": np.uint8}[dt]
     q = _c(w["q"], np.uint16)
     k = _c(w["k_pages"], raw)
     v = _c(w["v_pages"], raw)
@@ -93,6 +95,8 @@ def _common(w):
     sl = _c(w["seq_lens"], np.int32)
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
+    if dt in ("int4", "int2"):
+        assert k.shape[3] * 8 // {"int4": 4, "int2": 2}[dt] == D, "packed rows must hold head_dim codes"
     keep = (q, k, v, ks, vs, bt, sl)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
             _ptr(sl), B, T, Hq, Hkv, D, KV_DTYPES[dt]]
@@ -142,6 +146,12 @@ def verify_attn_partial(w, b, t, h, key_begin, key_end):
 
 def decode_e4m3(code: int) -> float:
     return _load().oracle_decode_e4m3(code)
+
+
+def decode_packed(data, idx: int, bits: int) -> float:
+    """Element idx of a packed byte array of `bits`-bit codes (4 or 2)."""
+    a = np.ascontiguousarray(data, np.uint8)
+    return _load().oracle_decode_packed(_ptr(a), int(idx), int(bits))
 
 
 def decode_bf16(bits: int) -> float:

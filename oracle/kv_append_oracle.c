@@ -18,6 +18,11 @@
  *   e4m3 code = round-to-nearest-even of clamp(y_d, -448, 448) (OCP e4m3:
  *               bias 7, 3 mantissa bits, subnormal step 2^-9, max 448)
  *   int8 code = clamp(round-half-even(y_d), -127, 127)
+ *   int4 / int2 code = clamp(round-half-even(y_d), -qmax, qmax) with qmax 7 / 1
+ *               (the int8 rule with fewer bits: the reading taken for the
+ *               "KVarN 4/2-bit KV cache" bullet of the 381 tps page, which
+ *               does not describe its format), packed two's complement, code
+ *               d at bit (d * bits) % 8 of byte d * bits / 8
  *
  * The two divisions are binary32 on purpose: the quantised code is an integer
  * decided by a floating-point quotient, and the definition fixes that quotient
@@ -25,14 +30,15 @@
  * round-to-nearest-even (the default mode), with no wider evaluation.
  *
  * Layouts (row-major): new rows uint16 (bf16 bits) [B, T, Hkv, D]; pages
- * [num_pages, 16, Hkv, D] of bf16 bits / e4m3 bytes / int8; scales float
+ * [num_pages, 16, Hkv, D] of bf16 bits / e4m3 bytes / int8, or [num_pages,
+ * 16, Hkv, D * bits / 8] packed bytes for int4 / int2; scales float
  * [num_pages, 16, Hkv]; block_table int32 [B, bt_stride]; seq_lens int32 [B].
  */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
 
-enum { APP_BF16 = 0, APP_E4M3 = 1, APP_INT8 = 2 };
+enum { APP_BF16 = 0, APP_E4M3 = 1, APP_INT8 = 2, APP_INT4 = 3, APP_INT2 = 4 };
 
 static float bf16_to_float(uint16_t bits)
 {
@@ -78,10 +84,43 @@ int8_t oracle_int8_encode(float y)
     return (int8_t)r;
 }
 
+/* 4-bit / 2-bit caches (the int8 rule with qmax 7 / 1): the integer code of
+ * y = x / s, round-half-even, clamped to +-qmax, stored as a two's-complement
+ * field at bit (d * bits) % 8 of byte d * bits / 8 of the row (the row's
+ * other fields are left as they are, then overwritten in turn). */
+static void append_row_packed(const uint16_t *x, int D, int bits, uint8_t *pages, float *scales, size_t row)
+{
+    const float qmax = (float)((1 << (bits - 1)) - 1);
+    float a = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        const float v = fabsf(bf16_to_float(x[d]));
+        if (v > a)
+            a = v;
+    }
+    const float s = a > 0.0f ? a / qmax : 1.0f;
+    uint8_t *dst = pages + row * (size_t)(D * bits / 8);
+    for (int d = 0; d < D; ++d) {
+        float r = rintf(bf16_to_float(x[d]) / s);
+        if (r > qmax)
+            r = qmax;
+        if (r < -qmax)
+            r = -qmax;
+        const int code = (int)r & ((1 << bits) - 1);
+        const int bit = (d * bits) % 8;
+        uint8_t *byte = dst + d * bits / 8;
+        *byte = (uint8_t)((*byte & ~(((1 << bits) - 1) << bit)) | (code << bit));
+    }
+    scales[row] = s;
+}
+
 static void append_row(const uint16_t *x, int D, int dtype, void *pages, float *scales, size_t row)
 {
     if (dtype == APP_BF16) {
         memcpy((uint16_t *)pages + row * (size_t)D, x, (size_t)D * sizeof(uint16_t));
+        return;
+    }
+    if (dtype == APP_INT4 || dtype == APP_INT2) {
+        append_row_packed(x, D, dtype == APP_INT4 ? 4 : 2, (uint8_t *)pages, scales, row);
         return;
     }
     float a = 0.0f;
@@ -118,7 +157,9 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, int B, int T,
 {
     if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens)
         return -1;
-    if (B < 1 || T < 1 || Hkv < 1 || D < 1 || bt_stride < 1 || dtype < APP_BF16 || dtype > APP_INT8)
+    if (B < 1 || T < 1 || Hkv < 1 || D < 1 || bt_stride < 1 || dtype < APP_BF16 || dtype > APP_INT2)
+        return -1;
+    if ((dtype == APP_INT4 && D % 2) || (dtype == APP_INT2 && D % 4))
         return -1;
     if (dtype != APP_BF16 && (!k_scale || !v_scale))
         return -1;

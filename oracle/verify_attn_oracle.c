@@ -21,7 +21,12 @@
  *   as bf16, fp8-e4m3 or int8 with one fp32 scale per (token, kv-head):
  *   "I pushed Qwen3.8-27B to 381 tps for a single request on a RTX 3090",
  *   "What we had" (fp8 KV cache) and "DFlash2 past 64k" (int8 cache, vLLM
- *   16-token blocks).
+ *   16-token blocks).  The same page's "KVarN 4/2-bit KV cache" bullet adds
+ *   4-bit and 2-bit caches without describing their format; the reading
+ *   used here is the int8 format with fewer bits: signed two's-complement
+ *   codes (int4 in [-8, 7], int2 in [-2, 1]; the encoder uses +-7 / +-1)
+ *   times the same per-(token, kv-head) fp32 scale, packed little-end first
+ *   (element d of a row sits in bits (d * bits) % 8 .. of byte d * bits / 8).
  *
  *   For sequence b, verify token t, query head h, kv head g = h / G:
  *     Khat[j] = decode(k_pages[page(j), j % 16, g, :]) * k_scale[page, slot, g]
@@ -32,7 +37,8 @@
  *
  * Layouts (row-major, contiguous):
  *   q           uint16 (bf16 bits) [B, T, Hq, D]
- *   k/v_pages   [num_pages, 16, Hkv, D] of bf16 bits / e4m3 bytes / int8
+ *   k/v_pages   [num_pages, 16, Hkv, D] of bf16 bits / e4m3 bytes / int8;
+ *               int4 / int2: [num_pages, 16, Hkv, D * bits / 8] packed bytes
  *   k/v_scale   float [num_pages, 16, Hkv]       (ignored for bf16)
  *   block_table int32 [B, bt_stride]
  *   seq_lens    int32 [B]   (includes the T verify tokens)
@@ -48,7 +54,7 @@
 
 #define ORACLE_PAGE 16
 
-enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1, ORACLE_INT8 = 2 };
+enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1, ORACLE_INT8 = 2, ORACLE_INT4 = 3, ORACLE_INT2 = 4 };
 
 /* bf16 is the top half of an IEEE-754 binary32. */
 double oracle_decode_bf16(uint16_t bits)
@@ -79,11 +85,25 @@ double oracle_decode_e4m3(uint8_t bits)
 
 double oracle_decode_int8(int8_t v) { return (double)v; }
 
+/* Element idx of a packed array of `bits`-bit two's-complement codes
+ * (bits = 4 or 2): the field at bit (idx * bits) % 8 of byte idx * bits / 8,
+ * sign-extended. */
+double oracle_decode_packed(const uint8_t *base, size_t idx, int bits)
+{
+    size_t bit = idx * (size_t)bits;
+    int field = (base[bit / 8] >> (bit % 8)) & ((1 << bits) - 1);
+    if (field >= (1 << (bits - 1)))
+        field -= 1 << bits;
+    return (double)field;
+}
+
 static double decode_elem(const void *base, size_t idx, int dtype)
 {
     switch (dtype) {
     case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)base)[idx]);
     case ORACLE_E4M3: return oracle_decode_e4m3(((const uint8_t *)base)[idx]);
+    case ORACLE_INT4: return oracle_decode_packed((const uint8_t *)base, idx, 4);
+    case ORACLE_INT2: return oracle_decode_packed((const uint8_t *)base, idx, 2);
     default: return oracle_decode_int8(((const int8_t *)base)[idx]);
     }
 }
@@ -181,7 +201,11 @@ static int check_problem(const problem *P)
         return -1;
     if (P->Hq % P->Hkv != 0)
         return -1;
-    if (P->dtype < ORACLE_BF16 || P->dtype > ORACLE_INT8)
+    if (P->dtype < ORACLE_BF16 || P->dtype > ORACLE_INT2)
+        return -1;
+    if (P->dtype == ORACLE_INT2 && P->D % 4 != 0)
+        return -1;
+    if (P->dtype == ORACLE_INT4 && P->D % 2 != 0)
         return -1;
     if (P->dtype != ORACLE_BF16 && (!P->k_scale || !P->v_scale))
         return -1;

@@ -14,7 +14,9 @@ Input recipe (the same for tests, smoke check and benchmark):
   ``a = max |x|`` over head_dim; fp8-e4m3 uses ``s = a / 448`` and stores
   ``e4m3(x / s)`` (round-to-nearest-even, clamped to +-448); int8 uses
   ``s = a / 127`` and stores ``clamp(rint(x / s), -127, 127)``; ``a == 0``
-  gives ``s = 1``.
+  gives ``s = 1``.  int4 / int2 follow int8 with ``qmax`` = 7 / 1 and pack the
+  two's-complement codes little-end first (element d at bit (d * bits) % 8 of
+  byte d * bits / 8): a row of head_dim codes is head_dim / 2 or / 4 bytes.
 * Paged cache: 16-token pages, page ids shuffled by the seed; a batch draws its
   pages from one shared pool assigned in order after the shuffle; slots past
   the end of a sequence are zero.
@@ -32,7 +34,21 @@ import numpy as np
 import torch
 
 PAGE = 16
-KV_ELEM_BYTES = {"bf16": 2, "fp8_e4m3": 1, "int8": 1}
+KV_ELEM_BYTES = {"bf16": 2, "fp8_e4m3": 1, "int8": 1}  # whole-byte formats
+KV_ELEM_BITS = {"bf16": 16, "fp8_e4m3": 8, "int8": 8, "int4": 4, "int2": 2}
+PACKED_QMAX = {"int4": 7, "int2": 1}
+
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Signed integer codes [..., D] -> packed bytes [..., D * bits / 8], code d
+    in bits (d * bits) % 8 .. of byte d * bits / 8 (two's complement)."""
+    per = 8 // bits
+    c = (codes.astype(np.int16) & ((1 << bits) - 1)).astype(np.uint8)
+    c = c.reshape(*codes.shape[:-1], codes.shape[-1] // per, per)
+    out = np.zeros(c.shape[:-1], np.uint8)
+    for k in range(per):
+        out |= (c[..., k] << (bits * k)).astype(np.uint8)
+    return out
 _CHUNK_TOKENS = 8192  # fixed draw granularity: keeps the stream reproducible
 
 
@@ -88,6 +104,12 @@ def _quantise(x: np.ndarray, kv_dtype: str):
     if kv_dtype == "bf16":
         return _bf16_bits(x), None
     a = np.max(np.abs(x), axis=-1).astype(np.float32)
+    if kv_dtype in PACKED_QMAX:
+        qm = PACKED_QMAX[kv_dtype]
+        s = np.where(a > 0, a / np.float32(qm), np.float32(1.0)).astype(np.float32)
+        y = (x / s[..., None]).astype(np.float32)
+        codes = np.clip(np.rint(y), -qm, qm).astype(np.int8)
+        return pack_codes(codes, KV_ELEM_BITS[kv_dtype]), s
     qmax = np.float32(448.0 if kv_dtype == "fp8_e4m3" else 127.0)
     s = np.where(a > 0, a / qmax, np.float32(1.0)).astype(np.float32)
     y = (x / s[..., None]).astype(np.float32)
@@ -138,15 +160,16 @@ def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peak
         block_table[b, :n] = perm[off:off + n]
         off += n
 
-    raw_dtype = np.uint16 if kv_dtype == "bf16" else (np.uint8 if kv_dtype == "fp8_e4m3" else np.int8)
-    k_pages = np.zeros((num_pages, PAGE, Hkv, D), raw_dtype)
-    v_pages = np.zeros((num_pages, PAGE, Hkv, D), raw_dtype)
+    raw_dtype = {"bf16": np.uint16, "fp8_e4m3": np.uint8, "int8": np.int8, "int4": np.uint8, "int2": np.uint8}[kv_dtype]
+    row_elems = D * KV_ELEM_BITS[kv_dtype] // 8 if kv_dtype in PACKED_QMAX else D
+    k_pages = np.zeros((num_pages, PAGE, Hkv, row_elems), raw_dtype)
+    v_pages = np.zeros((num_pages, PAGE, Hkv, row_elems), raw_dtype)
     quant = kv_dtype != "bf16"
     k_scale = np.zeros((num_pages, PAGE, Hkv), np.float32) if quant else None
     v_scale = np.zeros((num_pages, PAGE, Hkv), np.float32) if quant else None
     needle_pos = []
-    k_flat = k_pages.reshape(num_pages * PAGE, Hkv, D)
-    v_flat = v_pages.reshape(num_pages * PAGE, Hkv, D)
+    k_flat = k_pages.reshape(num_pages * PAGE, Hkv, row_elems)
+    v_flat = v_pages.reshape(num_pages * PAGE, Hkv, row_elems)
     for b, L in enumerate(seq_lens):
         k = _normal_rows(rng, L, Hkv, D)
         v = _normal_rows(rng, L, Hkv, D)
@@ -227,11 +250,11 @@ def algorithmic_bytes(w) -> int:
     kv head (plus its two scales when quantised), q, out (bf16), lse (fp32),
     the block-table entries in use and seq_lens.  Split partials excluded."""
     Hkv, D, T, Hq = w["Hkv"], w["D"], w["T"], w["Hq"]
-    eb = KV_ELEM_BYTES[w["kv_dtype"]]
+    row_bytes = D * KV_ELEM_BITS[w["kv_dtype"]] // 8
     quant = w["kv_dtype"] != "bf16"
     lens = np.asarray(w["seq_lens"], np.int64)
     B = len(lens)
-    kv = int(lens.sum()) * Hkv * (2 * D * eb + (8 if quant else 0))
+    kv = int(lens.sum()) * Hkv * (2 * row_bytes + (8 if quant else 0))
     pages = int(((lens + PAGE - 1) // PAGE).sum())
     return kv + 2 * (B * T * Hq * D * 2) + B * T * Hq * 4 + 4 * (pages + B)
 

@@ -138,6 +138,42 @@ def test_append_matches_independent_restatement(kv_dtype, D):
         assert np.array_equal(ks[~written], scale[~written])
 
 
+def packbits_codes(codes, bits):
+    """Signed codes [..., D] -> bytes [..., D * bits / 8] through numpy's
+    little-endian bit packing (independent of the oracle's shifts)."""
+    u = (codes.astype(np.int64) & ((1 << bits) - 1))
+    b = ((u[..., None] >> np.arange(bits)) & 1).astype(np.uint8)  # [..., D, bits], low bit first
+    return np.packbits(b.reshape(*codes.shape[:-1], -1), axis=-1, bitorder="little")
+
+
+@pytest.mark.parametrize("kv_dtype,bits,qmax", [("int4", 4, 7), ("int2", 2, 1)])
+@pytest.mark.parametrize("D", [64, 256])
+def test_append_packed_matches_independent_restatement(kv_dtype, bits, qmax, D):
+    """4-bit / 2-bit caches: every written row equals the int8 rule with
+    qmax 7 / 1 (binary32 absmax scale, round-half-even, clamp) packed with
+    numpy's bit packing; every other byte and scale is untouched."""
+    B, T, Hkv = 3, 5, 4
+    k_new, v_new, _, scale, bt, lens, num_pages = make_case(7 + D + bits, B, T, Hkv, D, "int8")
+    pages = np.full((num_pages, 16, Hkv, D * bits // 8), 0x5A, np.uint8)
+    kp, vp, ks, vs, skipped = oracle.kv_append(k_new, v_new, pages, pages, scale, scale, bt, lens, kv_dtype)
+    assert skipped == 0
+    written = np.zeros((num_pages, 16), bool)
+    for b in range(B):
+        for t in range(T):
+            pos = lens[b] - T + t
+            page, slot = bt[b, pos // 16], pos % 16
+            written[page, slot] = True
+            for src, dst, dsc in ((k_new, kp, ks), (v_new, vp, vs)):
+                x = bits_to_f32(src[b, t])  # [Hkv, D]
+                a = np.abs(x).max(axis=-1).astype(np.float32)
+                sc = np.where(a > 0, a / np.float32(qmax), np.float32(1.0)).astype(np.float32)
+                codes = np.clip(np.rint((x / sc[:, None]).astype(np.float32)), -qmax, qmax)
+                assert np.array_equal(dst[page, slot], packbits_codes(codes, bits))
+                assert np.array_equal(dsc[page, slot], sc)
+    assert np.array_equal(kp[~written], pages[~written]) and np.array_equal(vp[~written], pages[~written])
+    assert np.array_equal(ks[~written], scale[~written])
+
+
 @pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int8"])
 def test_append_invariants(kv_dtype):
     B, T, Hkv, D = 2, 16, 2, 128

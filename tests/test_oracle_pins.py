@@ -15,6 +15,19 @@ PAGE = 16
 
 
 # ---------------------------------------------------------------- helpers
+PACKED_BITS = {"int4": 4, "int2": 2}
+
+
+def unpack_codes(raw, bits, D):
+    """Packed bytes [..., D * bits / 8] -> signed codes [..., D], through
+    numpy's little-endian bit unpacking (a different route from the oracle's
+    shifts and masks): field d is bits d*bits .. d*bits+bits-1 of the row."""
+    b = np.unpackbits(np.ascontiguousarray(raw, np.uint8)[..., None], axis=-1, bitorder="little")
+    b = b.reshape(*raw.shape[:-1], D, bits).astype(np.int64)
+    u = (b * (1 << np.arange(bits))).sum(-1)
+    return np.where(u >= (1 << (bits - 1)), u - (1 << bits), u)
+
+
 def dense_kv(w, which):
     """Independent dequantisation with torch dtypes: [B][L_b, Hkv, D] float64."""
     raw = w[which + "_pages"]
@@ -24,6 +37,8 @@ def dense_kv(w, which):
         vals = t.view(torch.bfloat16).to(torch.float64)
     elif dt == "fp8_e4m3":
         vals = t.view(torch.float8_e4m3fn).to(torch.float64)
+    elif dt in PACKED_BITS:
+        vals = torch.from_numpy(unpack_codes(raw, PACKED_BITS[dt], w["D"]).astype(np.float64))
     else:
         vals = t.to(torch.float64)
     if dt != "bf16":
@@ -84,6 +99,37 @@ def test_e4m3_decoder_all_codes():
     assert oracle.decode_e4m3(0x01) == 2.0 ** -9  # smallest subnormal
 
 
+@pytest.mark.parametrize("bits", [4, 2])
+def test_packed_decoder_all_bytes(bits):
+    """Every byte value at every field position: the oracle's packed decoder
+    against numpy's bit unpacking and the two's-complement rule."""
+    data = np.arange(256, dtype=np.uint8)
+    per = 8 // bits
+    got = np.array([oracle.decode_packed(data, i, bits) for i in range(256 * per)])
+    ref = unpack_codes(data.reshape(256, 1), bits, per).reshape(-1)
+    assert np.array_equal(got, ref)
+    assert got.min() == -(1 << (bits - 1)) and got.max() == (1 << (bits - 1)) - 1
+
+
+@pytest.mark.parametrize("dt,qmax", [("int4", 7), ("int2", 1)])
+def test_packed_generator_round_trip(dt, qmax):
+    """Rows quantised by the input generator come back, through the oracle's
+    decoder, within half a code step: |x - code * s| <= s / 2, |code| <= qmax,
+    each row's largest |x| on a top code, an all-zero row on code 0."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    x = (rng.standard_normal((50, 64)) * rng.uniform(0.01, 30.0, (50, 1))).astype(np.float32)
+    x[7] = 0.0
+    raw, s = wl._quantise(x, dt)
+    bits = PACKED_BITS[dt]
+    codes = np.array([[oracle.decode_packed(raw[r], d, bits) for d in range(64)] for r in range(50)])
+    assert np.abs(codes).max() <= qmax
+    err = np.abs(x.astype(np.float64) - codes * s[:, None].astype(np.float64))
+    assert (err <= s[:, None] * (0.5 + 1e-6)).all()
+    nz = np.arange(50) != 7
+    assert (np.abs(codes[nz][np.arange(49), np.abs(x[nz]).argmax(1)]) == qmax).all()
+    assert (codes[7] == 0).all() and s[7] == 1.0
+
+
 def test_bf16_decoder_random_codes():
     rng = np.random.default_rng(1)
     codes = rng.integers(0, 1 << 16, size=4096, dtype=np.uint16)
@@ -95,7 +141,7 @@ def test_bf16_decoder_random_codes():
 
 
 # ---------------------------------------------------------------- brute force
-@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8", "int4", "int2"])
 @pytest.mark.parametrize("T,Hq,Hkv,D,lens", [
     (5, 4, 1, 64, [37]),
     (3, 6, 2, 16, [19, 40]),
@@ -118,12 +164,16 @@ def _set_all_v_to_one(w):
     elif dt == "fp8_e4m3":
         w["v_pages"][...] = 0x38  # 1.0 in e4m3
         w["v_scale"][...] = 1.0
+    elif dt in PACKED_BITS:  # code 1 in every field
+        bits = PACKED_BITS[dt]
+        w["v_pages"][...] = sum(1 << (bits * k) for k in range(8 // bits))
+        w["v_scale"][...] = 1.0
     else:
         w["v_pages"][...] = 1
         w["v_scale"][...] = 1.0
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8", "int4", "int2"])
 def test_softmax_rows_sum_to_one(dt):
     w = small_workload(7, [23, 64], 4, 6, 3, 32, dt)
     _set_all_v_to_one(w)
