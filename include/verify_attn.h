@@ -31,7 +31,11 @@
  *
  * Memory layouts (row-major, contiguous, all on the device unless noted):
  *     q            bf16  [B, T, Hq, D]
- *     k_pages      [num_pages, 16, Hkv, D] of bf16 / fp8-e4m3 / int8
+ *     k_pages      [num_pages, 16, Hkv, D] of bf16 / fp8-e4m3 / int8, or
+ *                  [num_pages, 16, Hkv, D * bits / 8] bytes for the packed
+ *                  4-bit / 2-bit caches: code d of a row is the two's-
+ *                  complement field at bit (d * bits) % 8 of byte
+ *                  d * bits / 8 (the first element in the low bits)
  *     v_pages      same layout as k_pages
  *     k_scale      fp32  [num_pages, 16, Hkv]   (one scale per token, kv head)
  *     v_scale      fp32  [num_pages, 16, Hkv]
@@ -42,6 +46,12 @@
  *     out          bf16  [B, T, Hq, D]
  *     lse          fp32  [B, T, Hq]   natural-log log-sum-exp of the scaled
  *                  scores (may be NULL when not wanted)
+ * The 4-bit and 2-bit caches follow the "KVarN 4/2-bit KV cache" bullet of
+ * "I pushed Qwen3.8-27B to 381 tps for a single request on a RTX 3090", which
+ * names the bit widths but not the format; the library takes the int8 rule
+ * with fewer bits (symmetric absmax scale per token and kv head, codes
+ * clamped to +-7 / +-1, decode = code * scale), so every cached format shares
+ * one definition of decode().
  * Row r of a kv head's packed tile is verify token t = r / G, query head
  * h = g*G + r % G.
  *
@@ -78,7 +88,9 @@ typedef struct va_plan va_plan;
 typedef enum {
     VA_BF16 = 0,     /* 2-byte bfloat16 cache, no scales */
     VA_FP8_E4M3 = 1, /* OCP fp8 e4m3, fp32 scale per (token, kv head) */
-    VA_INT8 = 2      /* int8, fp32 scale per (token, kv head) */
+    VA_INT8 = 2,     /* int8, fp32 scale per (token, kv head) */
+    VA_INT4 = 3,     /* 4-bit two's complement, two per byte, fp32 scale per (token, kv head) */
+    VA_INT2 = 4      /* 2-bit two's complement, four per byte, fp32 scale per (token, kv head) */
 } va_kv_dtype;
 
 typedef enum {
@@ -262,11 +274,14 @@ int verify_attn_noalloc_flags(int clear, int *flags, void *stream);
  *     pos  = L_b - T + t,  page = block_table[b][pos / 16],  slot = pos % 16
  *     x    = k_new[b, t, g, :]                (bf16, exact in fp32)
  *     a    = max_d |x_d|
- *     s    = a / qmax in fp32, qmax = 448 (e4m3) or 127 (int8); s = 1 if a = 0
+ *     s    = a / qmax in fp32, qmax = 448 (e4m3), 127 (int8), 7 (int4) or
+ *            1 (int2); s = 1 if a = 0
  *     y_d  = x_d / s in fp32 (correctly rounded)
  *     e4m3: byte_d = round-to-nearest-even e4m3 of clamp(y_d, -448, 448)
  *     int8: byte_d = clamp(round-half-even(y_d), -127, 127)
- *     k_pages[page, slot, g, :] = byte,  k_scale[page, slot, g] = s
+ *     int4 / int2: code_d = clamp(round-half-even(y_d), -qmax, qmax), packed
+ *           as the cache layout above states
+ *     k_pages[page, slot, g, :] = bytes,  k_scale[page, slot, g] = s
  * and the same for v.  A bf16 cache receives the bf16 bits unchanged (the
  * scale pointers are ignored and may be NULL).  This is the per-(token, kv
  * head) absmax quantisation the verify inputs are built with, so appending

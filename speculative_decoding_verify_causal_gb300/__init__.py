@@ -24,8 +24,8 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libverify_attn.so")
 
-VA_BF16, VA_FP8_E4M3, VA_INT8 = 0, 1, 2
-KV_DTYPE_CODES = {"bf16": VA_BF16, "fp8_e4m3": VA_FP8_E4M3, "int8": VA_INT8}
+VA_BF16, VA_FP8_E4M3, VA_INT8, VA_INT4, VA_INT2 = 0, 1, 2, 3, 4
+KV_DTYPE_CODES = {"bf16": VA_BF16, "fp8_e4m3": VA_FP8_E4M3, "int8": VA_INT8, "int4": VA_INT4, "int2": VA_INT2}
 VA_PATH_AUTO, VA_PATH_WARP, VA_PATH_MMA = 0, 1, 2
 PATH_CODES = {"auto": VA_PATH_AUTO, "warp": VA_PATH_WARP, "mma": VA_PATH_MMA}
 PAGE_SIZE = 16
@@ -247,6 +247,8 @@ def _kv_dtypes(code):
         return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
     if code == VA_FP8_E4M3:
         return (torch.uint8, torch.float8_e4m3fn)
+    if code in (VA_INT4, VA_INT2):  # packed bytes
+        return (torch.uint8, torch.int8)
     return (torch.int8,)
 
 
@@ -283,11 +285,15 @@ def verify_attn(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, T,
                 stream=None, kv_dtype=None):
     """Enqueue verify attention with this thread's current plan.  ``kv_dtype``
     only selects the accepted tensor dtypes for marshalling (inferred from
-    ``k_pages`` when omitted)."""
+    ``k_pages`` when omitted: a byte cache whose rows are D / 2 or D / 4 bytes
+    long is the 4-bit or 2-bit one)."""
     import torch
     if kv_dtype is None:
         kv_code = {torch.int8: VA_INT8, torch.uint8: VA_FP8_E4M3,
                    torch.float8_e4m3fn: VA_FP8_E4M3}.get(k_pages.dtype, VA_BF16)
+        if kv_code != VA_BF16 and k_pages.dim() == 4:
+            D = q.shape[-1]
+            kv_code = {D // 2: VA_INT4, D // 4: VA_INT2}.get(k_pages.shape[-1], kv_code)
     else:
         kv_code = _dtype_code(kv_dtype)
     args, tail, s = _marshal(kv_code, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,

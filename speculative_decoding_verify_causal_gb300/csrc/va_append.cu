@@ -1,16 +1,17 @@
 // KV append with quantise-on-write: the T verify tokens' K and V rows go into
 // the paged cache, quantised per (token, kv head) with an absmax fp32 scale
 // ("I pushed Qwen3.8-27B to 381 tps for a single request on a RTX 3090",
-// "DFlash2 past 64k": int8 cache in 16-token pages; "I pushed Qwen3.8-27B to
+// "DFlash2 past 64k": int8 cache in 16-token pages, and "KVarN 4/2-bit KV
+// cache", read as the int8 rule with 4 / 2 bits; "I pushed Qwen3.8-27B to
 // 124 tps on a single request on a RTX 3090", "What we had": fp8 cache).
 //
 // One warp per (k or v, sequence, token, kv head) row; lane l holds elements
 // [l E, l E + E) of the D-long row (E = D / 32).  The absmax is a warp
 // max-reduction (exact); the scale and the quotients are IEEE fp32 divisions
 // (__fdiv_rn), the e4m3 code is the hardware's round-to-nearest-even
-// saturating conversion and the int8 code a round-half-even conversion, so
+// saturating conversion and the integer codes a round-half-even conversion, so
 // every byte is the one the definition in verify_attn.h fixes.  HBM-bound:
-// 2 B read and 1 B (+ 4 B per row) written per element.
+// 2 B read and bits / 8 B (+ 4 B per row) written per element.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -74,6 +75,42 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
     if constexpr (DT == VA_BF16) {
         unsigned char *dst = static_cast<unsigned char *>(kv == 0 ? p.k_pages : p.v_pages);
         *reinterpret_cast<In *>(dst + (dst_row * D + lane * E) * 2) = raw;
+    } else if constexpr (DT == VA_INT4 || DT == VA_INT2) {
+        // 4-bit / 2-bit codes: the int8 rule with qmax 7 / 1, each lane's E
+        // codes packed into an F-bit field (element e at bit e * bits), then
+        // the fields of 32 / F neighbouring lanes ORed into one 32-bit word
+        // (lane order = element order, so the word is the row's little-endian
+        // bit stream) that the first of them stores.
+        constexpr int kBits = DT == VA_INT4 ? 4 : 2;
+        constexpr int qm = (1 << (kBits - 1)) - 1;
+        constexpr int F = E * kBits;          // 4 .. 32 bits per lane
+        constexpr int kLanesPerWord = 32 / F;
+        float x[E];
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            x[e] = __uint_as_float((uint32_t)h[e] << 16);
+            a = fmaxf(a, fabsf(x[e]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const float s = a > 0.f ? __fdiv_rn(a, (float)qm) : 1.f;
+        uint32_t field = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = max(-qm, min(qm, __float2int_rn(__fdiv_rn(x[e], s))));
+            field |= ((uint32_t)c & ((1u << kBits) - 1)) << (e * kBits);
+        }
+        uint32_t word = field;
+#pragma unroll
+        for (int k = 1; k < kLanesPerWord; ++k) {
+            const uint32_t nb = __shfl_down_sync(0xffffffffu, field, k);
+            if (lane + k < 32) word |= nb << (k * F);
+        }
+        unsigned char *dst = static_cast<unsigned char *>(kv == 0 ? p.k_pages : p.v_pages) +
+                             dst_row * (D * kBits / 8);
+        if (lane % kLanesPerWord == 0) *reinterpret_cast<uint32_t *>(dst + lane * F / 8) = word;
+        if (lane == 0) (kv == 0 ? p.k_scale : p.v_scale)[dst_row] = s;
     } else {
         float x[E];
         float a = 0.f;
@@ -119,7 +156,9 @@ cudaError_t launch_d(const AppendParams &p, int dtype, cudaStream_t s) {
     switch (dtype) {
     case VA_BF16: return launch_pdl(append_kernel<D, VA_BF16>, grid, dim3(kThreads), 0, s, p);
     case VA_FP8_E4M3: return launch_pdl(append_kernel<D, VA_FP8_E4M3>, grid, dim3(kThreads), 0, s, p);
-    default: return launch_pdl(append_kernel<D, VA_INT8>, grid, dim3(kThreads), 0, s, p);
+    case VA_INT8: return launch_pdl(append_kernel<D, VA_INT8>, grid, dim3(kThreads), 0, s, p);
+    case VA_INT4: return launch_pdl(append_kernel<D, VA_INT4>, grid, dim3(kThreads), 0, s, p);
+    default: return launch_pdl(append_kernel<D, VA_INT2>, grid, dim3(kThreads), 0, s, p);
     }
 }
 
@@ -135,7 +174,7 @@ extern "C" int verify_attn_kv_append(const void *k_new, const void *v_new, int n
     if (num_seqs < 1 || T < 1 || num_kv_heads < 1 || block_table_stride < 1 || num_pages < 0)
         return VA_ERR_INVALID_ARGUMENT;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return VA_ERR_UNSUPPORTED;
-    if (kv_dtype < VA_BF16 || kv_dtype > VA_INT8) return VA_ERR_UNSUPPORTED;
+    if (kv_dtype < VA_BF16 || kv_dtype > VA_INT2) return VA_ERR_UNSUPPORTED;
     if (kv_dtype != VA_BF16 && (!k_scale || !v_scale)) return VA_ERR_INVALID_ARGUMENT;
     auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
     if (misaligned(k_new) || misaligned(v_new) || misaligned(k_pages) || misaligned(v_pages))

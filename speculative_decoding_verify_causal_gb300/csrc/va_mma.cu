@@ -9,8 +9,9 @@
 // Qwen 3.8 decode", section "What I actually built" (lay the verify rows onto
 // the tensor instruction's row tile so the extra drafted tokens ride along
 // almost for free); the same section's advice to leave the data compressed
-// until the step before the tensor core is followed here: the cache stays 8-bit
-// from HBM into shared memory and is expanded right before the MMA.
+// until the step before the tensor core is followed here: the cache stays 8-,
+// 4- or 2-bit from HBM into shared memory and is expanded right before the
+// MMA.
 //
 // Per 64-key tile (4 pages):
 //   producer warp    stages the item's page ids, then TMA-gathers the pages
@@ -18,10 +19,10 @@
 //                    slot, kv head, d], one box per page) into a ring of raw
 //                    stages, K then V of every tile (the first stage of each
 //                    slot already during set-up);
-//   dequant warps    (fp8-e4m3 / int8) two groups of four, one taking the K
-//                    tile and one the V tile of every tile: a raw stage goes
-//                    to registers and back to the producer, then fp16 -- both
-//                    conversions are exact -- into the 128-byte-swizzled
+//   dequant warps    (fp8-e4m3 / int8 / int4 / int2) two groups of four, one
+//                    taking the K tile and one the V tile of every tile: a raw
+//                    stage goes to registers and back to the producer, then
+//                    fp16 -- every conversion is exact -- into the 128-byte-swizzled
 //                    layout the MMA reads; the K group also carries each
 //                    key's k and v scale (loaded two tiles ahead) into a ring
 //                    the softmax reads (bf16 caches are TMA'd straight into
@@ -64,7 +65,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = kMmaTile;     // keys per S tile (MMA N)
-constexpr int kMaxRawStages = 6;    // raw (8-bit) stages: one 64-key K or V tile each
+constexpr int kMaxRawStages = 6;    // raw (as cached) stages: one 64-key K or V tile each
 constexpr int kMinRawStages = 3;
 constexpr int kBfStages = 3;        // bf16: 64-key stages TMA'd straight into MMA layout
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -90,7 +91,9 @@ struct Cfg {
     static constexpr int kNumBuf = kQuant ? 2 : (D == 256 ? 2 : kBfStages);  // 64 KB bf16 stages at D = 256
     static constexpr int kConvBytes = kTile * D * 2;   // K or V tile, 16-bit, SW128 chunks of 64 d
     static constexpr int kChunkBytes = kTile * 128;    // one 64-d chunk of a tile
-    static constexpr int kRawTileBytes = kTile * D;    // one K or V tile, 8-bit
+    static constexpr int kBits = DT == VA_BF16 ? 16 : DT == VA_INT4 ? 4 : DT == VA_INT2 ? 2 : 8;
+    static constexpr int kRowBytes = D * kBits / 8;    // one cached row (token, kv head)
+    static constexpr int kRawTileBytes = kTile * kRowBytes;  // one K or V tile as cached
     // warps 0-7 softmax (two per TMEM lane quarter), 8-15 dequant (quantised
     // caches only: 8-11 K, 12-15 V), then the producer and the MMA issuer
     static constexpr int kSoftmaxWarps = 8;
@@ -227,6 +230,84 @@ __device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t w, uint32_t &lo, uint
     hi = *reinterpret_cast<uint32_t *>(&b);
 }
 
+// 4-bit codes -> fp16, exact, the same magic-number idea: code k of w sits in
+// bits [4k, 4k + 4); a nibble n of a two's-complement code c has n ^ 8 = c + 8
+// in [0, 16), so (n ^ 8) | 0x6400 is the fp16 1024 + c + 8 and subtracting
+// 1032 leaves c.  One mask-and-xor makes the pairs (c_s, c_s+4); byte
+// permutes put them in element order.  h[j] = (c_2j, c_2j+1).
+__device__ __forceinline__ void int4x8_to_half2x4(uint32_t w, uint32_t (&h)[4]) {
+    uint32_t a[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) a[s] = ((w >> (4 * s)) & 0x000F000Fu) ^ 0x64086408u;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(h[0]) : "r"(a[0]), "r"(a[1]));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(h[1]) : "r"(a[2]), "r"(a[3]));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(h[2]) : "r"(a[0]), "r"(a[1]));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(h[3]) : "r"(a[2]), "r"(a[3]));
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h[j]), bias);
+        h[j] = *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+// 2-bit codes -> fp16, exact: code k of w in bits [2k, 2k + 2), (n ^ 2) = c + 2
+// in [0, 4), bias 1026; pairs (c_s, c_s+8) permuted into element order.
+__device__ __forceinline__ void int2x16_to_half2x8(uint32_t w, uint32_t (&h)[8]) {
+    uint32_t a[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) a[s] = ((w >> (2 * s)) & 0x00030003u) ^ 0x64026402u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(h[j]) : "r"(a[2 * j]), "r"(a[2 * j + 1]));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(h[4 + j]) : "r"(a[2 * j]), "r"(a[2 * j + 1]));
+    }
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6402), __ushort_as_half(0x6402));  // 1026
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h[j]), bias);
+        h[j] = *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+// The 16 elements of one raw piece of a quantised cache row -> 8 fp16 pairs
+// in element order.  A piece is 16 / 8 / 4 bytes (8-bit / 4-bit / 2-bit).
+template <int DT>
+struct RawPiece {
+    static constexpr int kWords = DT == VA_INT4 ? 2 : DT == VA_INT2 ? 1 : 4;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(uint32_t a) {
+        if constexpr (kWords == 4) {
+            const uint4 v = lds_u4(a);
+            w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+        } else if constexpr (kWords == 2) {
+            const uint2 v = lds_u2(a);
+            w[0] = v.x, w[1] = v.y;
+        } else {
+            w[0] = lds_u32(a);
+        }
+    }
+    __device__ __forceinline__ void to_half(uint32_t (&hw)[8]) const {
+        if constexpr (DT == VA_INT2) {
+            int2x16_to_half2x8(w[0], hw);
+        } else if constexpr (DT == VA_INT4) {
+            uint32_t a[4], b[4];
+            int4x8_to_half2x4(w[0], a);
+            int4x8_to_half2x4(w[1], b);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hw[j] = a[j], hw[4 + j] = b[j];
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (DT == VA_INT8)
+                    int8x4_to_half2x2(w[k], hw[2 * k], hw[2 * k + 1]);
+                else
+                    e4m3x4_to_half2x2(w[k], hw[2 * k], hw[2 * k + 1]);
+            }
+        }
+    }
+};
+
 // Byte offset of 16-byte unit u (0..7) of tile row `row` inside a 64-d chunk
 // of a 128-byte-swizzled tile (rows of 128 bytes, 8-row / 1024-byte atoms).
 __device__ __forceinline__ uint32_t sw128(int row, int u) { return row * 128 + ((u ^ (row & 7)) << 4); }
@@ -274,7 +355,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         const int slot = ps % nst, i = ps >> 1, kv = ps & 1;
         const int npg = tile_npg(i);
         const int page = tile_page(i);
-        const uint32_t page_bytes = VA_PAGE_SIZE * D;  // one page, one head, 8-bit
+        const uint32_t page_bytes = VA_PAGE_SIZE * C::kRowBytes;  // one page, one head, as cached
         if (lane == 0) mbar_arrive_expect_tx(bar(kRawFull + slot), npg * page_bytes);
         __syncwarp();
         if (lane < npg)
@@ -846,15 +927,17 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
         // Two groups of four warps, one per lane quarter each: warps 8-11 take
         // the K tile of every tile (plus this head's k and v scales, which the
         // softmax of the tile needs), warps 12-15 the V tile, so that the K
-        // pass of tile i+1 runs beside the V pass of tile i.  int8 / e4m3 ->
-        // fp16 (exact) into the MMA layout.
+        // pass of tile i+1 runs beside the V pass of tile i.  int8 / e4m3 /
+        // int4 / int2 -> fp16 (exact) into the MMA layout; each thread takes
+        // pieces of 16 consecutive elements, whatever their width in bytes.
         constexpr int kGT = C::kDequantWarps * 16;             // threads per group
         const int dq = tid - C::kSoftmaxWarps * 32;            // 0 .. 2 kGT - 1
         const int kv = dq / kGT;                               // 0: K group, 1: V group
         const int dt = dq % kGT;
         const uint32_t ring = sbase + L.scale_ring;
-        constexpr int kChunks = kTile * D / 16;                // 16-byte raw chunks per tile
+        constexpr int kChunks = kTile * D / 16;                // 16-element raw pieces per tile
         constexpr int kPer = kChunks / kGT;                    // per thread (2, 4 or 8)
+        constexpr int kPieceBytes = 16 * C::kBits / 8;          // 16, 8 or 4
         constexpr int kRowStep = kGT * 16 / D;                 // tile rows between a thread's chunks
         static_assert(kPer * kGT == kChunks && kRowStep % 8 == 0, "chunks must divide evenly");
         // this thread's chunks sit kGT * 16 raw bytes (kRowStep rows, a
@@ -894,11 +977,11 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
                 ok = false;
                 break;
             }
-            const uint32_t st = sbase + L.raw + slot * L.raw_stride + dt * 16;
+            const uint32_t st = sbase + L.raw + slot * L.raw_stride + dt * kPieceBytes;
             const uint32_t dst = sbase + (kv == 0 ? L.conv_k : L.conv_v) + buf * C::kConvBytes;
-            uint4 raw[kPer];
+            RawPiece<DT> raw[kPer];
 #pragma unroll
-            for (int jj = 0; jj < kPer; ++jj) raw[jj] = lds_u4(st + jj * kGT * 16);
+            for (int jj = 0; jj < kPer; ++jj) raw[jj].load(st + jj * kGT * kPieceBytes);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kRawEmpty + slot));
             // the tile's scales move up the pipeline and the load two tiles
@@ -917,14 +1000,7 @@ mma_partial_kernel(const __grid_constant__ MmaParams mp) {
 #pragma unroll
             for (int jj = 0; jj < kPer; ++jj) {
                 uint32_t hw[8];
-                const uint32_t rw[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (DT == VA_INT8)
-                        int8x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
-                    else
-                        e4m3x4_to_half2x2(rw[k], hw[2 * k], hw[2 * k + 1]);
-                }
+                raw[jj].to_half(hw);
                 uint4 lo = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 uint4 hi = make_uint4(hw[4], hw[5], hw[6], hw[7]);
                 if (n0 + jj * kRowStep >= nvalid) lo = hi = make_uint4(0, 0, 0, 0);  // past the split end
@@ -999,15 +1075,20 @@ bool make_part_map(CUtensorMap *m, float *o_part, int D, int rows_per_group, int
     return r == CUDA_SUCCESS;
 }
 
-// 4-D view of a page pool [pages, 16, Hkv, D]: dims innermost first.
-bool make_map(CUtensorMap *m, const void *base, int D, int Hkv, int num_pages, bool bf16) {
+// 4-D view of a page pool [pages, 16, Hkv, row]: dims innermost first.  A
+// bf16 row is D elements (boxes of 64, swizzled into the MMA layout); a
+// quantised row is its D * bits / 8 bytes (one box per page and head: 16, 32,
+// 64, 128 or 256 bytes wide, always a multiple of 16).
+bool make_map(CUtensorMap *m, const void *base, int D, int bits, int Hkv, int num_pages) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const bool bf16 = bits == 16;
     const cuuint64_t eb = bf16 ? 2 : 1;
+    const cuuint64_t row = bf16 ? (cuuint64_t)D : (cuuint64_t)D * bits / 8;  // elements of the map's type
     const cuuint64_t pages = num_pages > 0 ? (cuuint64_t)num_pages : (cuuint64_t)1 << 30;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)VA_PAGE_SIZE, pages};
-    cuuint64_t strides[3] = {D * eb, (cuuint64_t)Hkv * D * eb, (cuuint64_t)VA_PAGE_SIZE * Hkv * D * eb};
-    cuuint32_t box[4] = {bf16 ? 64u : (cuuint32_t)D, 1u, (cuuint32_t)VA_PAGE_SIZE, 1u};
+    cuuint64_t dims[4] = {row, (cuuint64_t)Hkv, (cuuint64_t)VA_PAGE_SIZE, pages};
+    cuuint64_t strides[3] = {row * eb, (cuuint64_t)Hkv * row * eb, (cuuint64_t)VA_PAGE_SIZE * Hkv * row * eb};
+    cuuint32_t box[4] = {bf16 ? 64u : (cuuint32_t)row, 1u, (cuuint32_t)VA_PAGE_SIZE, 1u};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
                      const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1020,9 +1101,8 @@ template <int D, int DT>
 cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
     MmaParams mp;
     mp.p = p;
-    const bool bf16 = DT == VA_BF16;
-    if (!make_map(&mp.tm_k, p.k_pages, D, p.Hkv, p.num_pages, bf16) ||
-        !make_map(&mp.tm_v, p.v_pages, D, p.Hkv, p.num_pages, bf16))
+    if (!make_map(&mp.tm_k, p.k_pages, D, Cfg<D, DT>::kBits, p.Hkv, p.num_pages) ||
+        !make_map(&mp.tm_v, p.v_pages, D, Cfg<D, DT>::kBits, p.Hkv, p.num_pages))
         return cudaErrorInvalidValue;
     memset(&mp.tm_o, 0, sizeof(mp.tm_o));
     if (p.num_parts > 0 && !make_part_map(&mp.tm_o, p.o_part, D, p.rows_per_group, p.num_parts))
@@ -1047,7 +1127,9 @@ cudaError_t launch_d(const PartialParams &p, int dtype, int n, cudaStream_t s) {
     switch (dtype) {
     case VA_BF16: return launch_one<D, VA_BF16>(p, n, s);
     case VA_FP8_E4M3: return launch_one<D, VA_FP8_E4M3>(p, n, s);
-    default: return launch_one<D, VA_INT8>(p, n, s);
+    case VA_INT8: return launch_one<D, VA_INT8>(p, n, s);
+    case VA_INT4: return launch_one<D, VA_INT4>(p, n, s);
+    default: return launch_one<D, VA_INT2>(p, n, s);
     }
 }
 

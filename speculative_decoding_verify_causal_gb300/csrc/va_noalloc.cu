@@ -131,7 +131,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     if (!seq_lens_host || B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv)
         return VA_ERR_INVALID_ARGUMENT;
     if (D != 64 && D != 128 && D != 256) return VA_ERR_UNSUPPORTED;
-    if (kv_dtype < VA_BF16 || kv_dtype > VA_INT8) return VA_ERR_UNSUPPORTED;
+    if (kv_dtype < VA_BF16 || kv_dtype > VA_INT2) return VA_ERR_UNSUPPORTED;
     if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out)
         return VA_ERR_INVALID_ARGUMENT;
     if (kv_dtype != VA_BF16 && (!k_scale || !v_scale)) return VA_ERR_INVALID_ARGUMENT;

@@ -53,7 +53,10 @@ struct Geometry {
 
 int head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
-int kv_bytes(int dtype) { return dtype == VA_BF16 ? 2 : 1; }
+// Bits per cached element.
+int kv_bits(int dtype) {
+    return dtype == VA_BF16 ? 16 : dtype == VA_INT4 ? 4 : dtype == VA_INT2 ? 2 : 8;
+}
 
 // Splits of one sequence for a nominal split length c: equal parts rounded up
 // to the key tile, so every split but the last is a whole number of tiles.
@@ -86,7 +89,7 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
     if (!seq_lens || B < 1 || T < 1 || Hq < 1 || Hkv < 1) return VA_ERR_INVALID_ARGUMENT;
     if (Hq % Hkv != 0) return VA_ERR_INVALID_ARGUMENT;
     if (!head_dim_ok(D)) return VA_ERR_UNSUPPORTED;
-    if (dtype < VA_BF16 || dtype > VA_INT8) return VA_ERR_UNSUPPORTED;
+    if (dtype < VA_BF16 || dtype > VA_INT2) return VA_ERR_UNSUPPORTED;
     int max_pages = 0;
     for (int b = 0; b < B; ++b) {
         if (seq_lens[b] < T) return VA_ERR_INVALID_ARGUMENT;
@@ -137,7 +140,7 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
     // Cost model in key-token units: a fixed start-up cost per item (q load,
     // pipeline fill) and, for split sequences, the partial write + combine
     // read of rows x D fp32 relative to one token's KV bytes.
-    const double token_bytes = 2.0 * D * kv_bytes(dtype) + (dtype == VA_BF16 ? 0 : 8);
+    const double token_bytes = 2.0 * D * kv_bits(dtype) / 8.0 + (dtype == VA_BF16 ? 0 : 8);
     const double c_item = mma ? 384.0 : 128.0;
     const double c_split = 2.0 * g.rows_per_group * (D + 1) * 4.0 / token_bytes;
 

@@ -10,8 +10,9 @@
 // Qwen3.8-27B to 124 tps on a single request on a RTX 3090", bullet
 // "Split-KV attention kernel for the verify step").  Per 32-key tile:
 //   1. the 32 K and V rows are gathered through the block table (16-byte
-//      loads), dequantised (fp8-e4m3 / int8 times the per-token scale, or
-//      bf16) and staged in shared memory as fp32;
+//      loads; 8 / 4 bytes for the 4-bit / 2-bit caches), dequantised
+//      (fp8-e4m3 / int8 / int4 / int2 times the per-token scale, or bf16) and
+//      staged in shared memory as fp32;
 //   2. lane j of each warp scores key j against the warp's rows, applies the
 //      bottom-right causal mask (verify token t sees keys j <= L - T + t) and
 //      updates the row's running max / sum with shuffles (online softmax in
@@ -80,6 +81,44 @@ __device__ __forceinline__ void decode16<VA_INT8>(const uint4 &raw, float *dst, 
             dst[4 * i + k] = static_cast<float>(static_cast<int8_t>(w[i] >> (8 * k))) * scale;
 }
 
+// 4-bit / 2-bit caches: 16 codes in 8 / 4 bytes (raw.x, raw.y), code k of a
+// word in bits [k bits, (k + 1) bits), sign-extended by an arithmetic shift.
+template <>
+__device__ __forceinline__ void decode16<VA_INT4>(const uint4 &raw, float *dst, float scale) {
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            dst[8 * i + k] = static_cast<float>(static_cast<int32_t>(w[i] << (28 - 4 * k)) >> 28) * scale;
+}
+
+template <>
+__device__ __forceinline__ void decode16<VA_INT2>(const uint4 &raw, float *dst, float scale) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        dst[k] = static_cast<float>(static_cast<int32_t>(raw.x << (30 - 2 * k)) >> 30) * scale;
+}
+
+// Bits per cached element, and the raw bytes holding one decode16 chunk.
+template <int DT>
+__host__ __device__ constexpr int elem_bits() {
+    return DT == VA_BF16 ? 16 : DT == VA_INT4 ? 4 : DT == VA_INT2 ? 2 : 8;
+}
+
+// One chunk of a cache row as 16 / 8 / 4 aligned bytes (unused words zero).
+template <int BYTES>
+__device__ __forceinline__ uint4 load_chunk(const uint8_t *src) {
+    if constexpr (BYTES == 16) {
+        return *reinterpret_cast<const uint4 *>(src);
+    } else if constexpr (BYTES == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        return make_uint4(v.x, v.y, 0u, 0u);
+    } else {
+        return make_uint4(*reinterpret_cast<const uint32_t *>(src), 0u, 0u, 0u);
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -102,8 +141,9 @@ template <int D, int DT>
 __global__ void __launch_bounds__(kThreads) warp_partial_kernel(const PartialParams p) {
     constexpr int RB = kWarpRows;
     constexpr int TK = kWarpTile;
-    constexpr int EB = DT == VA_BF16 ? 2 : 1;       // bytes per cached element
-    constexpr int EPC = 16 / EB;                    // elements per 16-byte chunk
+    constexpr int EPC = DT == VA_BF16 ? 8 : 16;     // elements per decoded chunk
+    constexpr int CB = EPC * elem_bits<DT>() / 8;   // raw bytes per chunk (16, 8 or 4)
+    constexpr int RB_BYTES = D * elem_bits<DT>() / 8;  // bytes per cache row
     constexpr int CPR = D / EPC;                    // chunks per cache row
     constexpr int DPT = (D + kThreads - 1) / kThreads;  // head_dim slice per thread
     // programmatic dependent launch: nothing of the caller's is touched before this
@@ -177,8 +217,8 @@ __global__ void __launch_bounds__(kThreads) warp_partial_kernel(const PartialPar
             if (Valid[j]) {
                 const int page = bt[key / VA_PAGE_SIZE];
                 const size_t row = ((size_t)page * VA_PAGE_SIZE + key % VA_PAGE_SIZE) * Hkv + it.kvh;
-                const uint4 kr = *reinterpret_cast<const uint4 *>(kbase + (row * D + part * EPC) * EB);
-                const uint4 vr = *reinterpret_cast<const uint4 *>(vbase + (row * D + part * EPC) * EB);
+                const uint4 kr = load_chunk<CB>(kbase + row * RB_BYTES + part * CB);
+                const uint4 vr = load_chunk<CB>(vbase + row * RB_BYTES + part * CB);
                 const float ks = DT == VA_BF16 ? 1.f : p.k_scale[row];
                 const float vs = DT == VA_BF16 ? 1.f : p.v_scale[row];
                 decode16<DT>(kr, kf, ks);
@@ -297,7 +337,9 @@ cudaError_t launch_d(const PartialParams &p, int dtype, int n, cudaStream_t s) {
     switch (dtype) {
     case VA_BF16: return launch_one<D, VA_BF16>(p, n, s);
     case VA_FP8_E4M3: return launch_one<D, VA_FP8_E4M3>(p, n, s);
-    default: return launch_one<D, VA_INT8>(p, n, s);
+    case VA_INT8: return launch_one<D, VA_INT8>(p, n, s);
+    case VA_INT4: return launch_one<D, VA_INT4>(p, n, s);
+    default: return launch_one<D, VA_INT2>(p, n, s);
     }
 }
 

@@ -224,8 +224,9 @@ def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peak
     }
 
 
-def config_workload(name: str):
-    """One of the five named configurations, fully materialised."""
+def config_workload(name: str, kv_dtype: str | None = None):
+    """One of the five named configurations, fully materialised; ``kv_dtype``
+    replaces its cache type (same seed, shapes and needles)."""
     c = CONFIGS[name]
     seed = 20260 + c.index
     if c.batch > 1:
@@ -241,8 +242,8 @@ def config_workload(name: str):
     elif c.needles == "depths":
         def needles(rng, b, L, ctx=c.seq_lens[0]):
             return [int(math.floor(p * ctx)) for p in (0.10, 0.50, 0.90, 0.99)]
-    return make_workload(seed, seq_lens, c.T, c.Hq, c.Hkv, c.D, c.kv_dtype,
-                         needles=needles, peaks=c.peaks, name=name)
+    return make_workload(seed, seq_lens, c.T, c.Hq, c.Hkv, c.D, kv_dtype or c.kv_dtype,
+                         needles=needles, peaks=c.peaks, name=name if kv_dtype is None else f"{name}/{kv_dtype}")
 
 
 def algorithmic_bytes(w) -> int:

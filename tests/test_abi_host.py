@@ -78,6 +78,8 @@ def _check_cover(lens, T, Hq, Hkv, items, info):
     ([262160], 16, 24, 4, 256, "int8"),
     (list(np.random.default_rng(3).integers(1000, 8001, 64) + 5), 5, 24, 4, 256, "fp8_e4m3"),
     ([1, 2, 3, 17, 33], 1, 8, 8, 128, "bf16"),
+    ([262160], 16, 24, 4, 256, "int4"),
+    ([3005, 705, 17], 5, 24, 4, 64, "int2"),
 ])
 @pytest.mark.parametrize("path", ["warp", "mma", "auto"])
 def test_planner_covers_every_key_once(lens, T, Hq, Hkv, D, dt, path):
@@ -127,6 +129,7 @@ def test_planner_forced_split_length():
     (dict(seq_lens=[4], T=5), va.VerifyAttnError),                      # L < T
     (dict(Hq=6, Hkv=4), va.VerifyAttnError),                            # Hq % Hkv
     (dict(D=96), va.VerifyAttnError),                                   # unsupported head_dim
+    (dict(dt=5), va.VerifyAttnError),                                   # unknown cache type
     (dict(block_table_stride=1, seq_lens=[100]), va.VerifyAttnError),   # stride < pages
 ])
 def test_planner_rejects_bad_arguments(kw, code):

@@ -41,7 +41,7 @@ def run_gpu(k_new, v_new, pages, scale, bt, lens, T, kv_dtype, num_pages=0):
 
 
 CASES = [(B, T, Hkv, D, dt) for (B, T, Hkv) in ((1, 1, 1), (3, 5, 4), (2, 16, 4), (64, 5, 4))
-         for D in (64, 128, 256) for dt in ("fp8_e4m3", "int8", "bf16")]
+         for D in (64, 128, 256) for dt in ("fp8_e4m3", "int8", "bf16", "int4", "int2")]
 
 
 @pytest.mark.parametrize("B,T,Hkv,D,kv_dtype", CASES)
@@ -56,7 +56,7 @@ def test_kv_append_bit_exact(B, T, Hkv, D, kv_dtype):
         assert np.array_equal(vs.view(np.uint32), rvs.view(np.uint32))
 
 
-@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int8"])
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "int8", "int4", "int2"])
 def test_kv_append_extreme_rows(kv_dtype):
     """Rows of ties, tiny (subnormal-scale) and huge magnitudes, all-equal rows."""
     B, T, Hkv, D = 1, 8, 2, 64

@@ -74,7 +74,7 @@ def test_full_size_configs_full_output(name):
 
 # ------------------------------------------------------------ non-unit scales
 SCALED = [(k, v, dt, T, G) for (k, v) in ((1e-3, 1e-3), (30.0, 30.0), (1.0, 1e-4), (1.0, 30.0), (30.0, 1e-4))
-          for dt in ("int8", "fp8_e4m3") for (T, G) in ((16, 6), (1, 4))]
+          for dt in ("int8", "fp8_e4m3", "int4", "int2") for (T, G) in ((16, 6), (1, 4))]
 
 
 @pytest.mark.parametrize("k_std,v_std,dt,T,G", SCALED)
@@ -90,6 +90,38 @@ def test_non_unit_scales(k_std, v_std, dt, T, G):
     ref_out, ref_lse = oracle.verify_attn(w)
     stats = compare(out, lse, ref_out, ref_lse, f"k_std {k_std} v_std {v_std} {dt} {info}", v_std=v_std)
     print(f"k_std {k_std} v_std {v_std} {dt} T{T} G{G}: {stats}")
+
+
+# ------------------------------------------------------------ 4-bit / 2-bit caches
+PACKED = [(T, G, D, dt) for dt in ("int4", "int2") for (T, G) in ((1, 4), (5, 4), (16, 6), (8, 8))
+          for D in (64, 128, 256)]
+
+
+@pytest.mark.parametrize("path", ["warp", "mma"])
+@pytest.mark.parametrize("T,G,D,dt", PACKED)
+def test_packed_cache_shapes(T, G, D, dt, path):
+    """The 4-bit / 2-bit caches (the int8 rule with codes +-7 / +-1, packed
+    low bits first) in both kernels, every head width: the shortest possible
+    sequence, one page + T, ragged tails and a split sequence."""
+    lens = [T, 16 + T, 203, 1200 + T]
+    w = wl.make_workload(5000 + 97 * T + 13 * G + D + len(dt), lens, T, G * 2, 2, D, dt, extra_pages=2)
+    out, lse, info = run_gpu(w, {"tokens_per_split": 128, "path": path})
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"T{T} G{G} D{D} {dt} {path} {info}")
+
+
+@pytest.mark.parametrize("dt", ["int4", "int2"])
+def test_maxctx_packed_full_output(dt):
+    """262144 + 16 cached tokens (24 q / 4 kv heads, D = 256, needles at
+    10/50/90/99 % depth) in a 4-bit / 2-bit cache: every output row against
+    the oracle, in the default plan (tensor cores, one split per SM)."""
+    w = wl.config_workload("maxctx", kv_dtype=dt)
+    out, lse, info = run_gpu(w)
+    assert info["path"] == 2 and info["max_splits"] > 1
+    ref_out, ref_lse = oracle.verify_attn(w)
+    stats = compare(out, lse, ref_out, ref_lse, f"maxctx {dt} {info}")
+    print(f"maxctx/{dt}: {stats}")
+    assert stats["ulp_allowance_used"] <= 1e-3 * stats["elements"], stats
 
 
 # ------------------------------------------------------------ long contexts, other dtypes / widths

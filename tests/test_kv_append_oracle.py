@@ -105,6 +105,10 @@ def make_case(seed, B, T, Hkv, D, kv_dtype, extra_pages=3):
     if kv_dtype == "bf16":
         pages = np.full((num_pages, 16, Hkv, D), 0x1234, np.uint16)
         scale = None
+    elif kv_dtype in ("int4", "int2"):  # packed bytes, D * bits / 8 per row
+        bits = 4 if kv_dtype == "int4" else 2
+        pages = np.full((num_pages, 16, Hkv, D * bits // 8), 0x5A, np.uint8)
+        scale = np.full((num_pages, 16, Hkv), 7.0, np.float32)
     else:
         pages = np.full((num_pages, 16, Hkv, D), 0x5A, np.int8 if kv_dtype == "int8" else np.uint8)
         scale = np.full((num_pages, 16, Hkv), 7.0, np.float32)
@@ -153,8 +157,8 @@ def test_append_packed_matches_independent_restatement(kv_dtype, bits, qmax, D):
     qmax 7 / 1 (binary32 absmax scale, round-half-even, clamp) packed with
     numpy's bit packing; every other byte and scale is untouched."""
     B, T, Hkv = 3, 5, 4
-    k_new, v_new, _, scale, bt, lens, num_pages = make_case(7 + D + bits, B, T, Hkv, D, "int8")
-    pages = np.full((num_pages, 16, Hkv, D * bits // 8), 0x5A, np.uint8)
+    k_new, v_new, pages, scale, bt, lens, num_pages = make_case(7 + D + bits, B, T, Hkv, D, kv_dtype)
+    assert pages.shape == (num_pages, 16, Hkv, D * bits // 8) and pages.dtype == np.uint8
     kp, vp, ks, vs, skipped = oracle.kv_append(k_new, v_new, pages, pages, scale, scale, bt, lens, kv_dtype)
     assert skipped == 0
     written = np.zeros((num_pages, 16), bool)
