@@ -47,6 +47,10 @@ def parse_args():
     ap.add_argument("--config", default="lookup16",
                     help="tiny | mtp4 | lookup16 | batched | maxctx")
     ap.add_argument("--path", default="auto", choices=["auto", "warp", "mma"])
+    ap.add_argument("--kv-dtype", default=None, help="replace the configuration's cache type "
+                    "(bf16 | fp8_e4m3 | int8 | int4 | int2)")
+    ap.add_argument("--T", type=int, default=None, help="replace the configuration's verify tokens")
+    ap.add_argument("--Hq", type=int, default=None, help="replace the configuration's query heads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
@@ -214,7 +218,7 @@ def run_reference(args):
         return 0
     from speculative_decoding_verify_causal_gb300 import workloads as wl
     import oracle
-    w = wl.config_workload(args.config)
+    w = wl.config_workload(args.config, args.kv_dtype, args.T, args.Hq)
     cores = oracle.max_threads(0)
     B, T, Hq = w["q"].shape[:3]
     all_rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
@@ -241,7 +245,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.config}: {wl.CONFIGS[args.config].description}",
+        "config": {"workload": f"{wl.variant_name(args.config, args.kv_dtype, args.T, args.Hq)}: "
+                               f"{wl.describe(args.config, args.kv_dtype, args.T, args.Hq)}",
                    "step": f"{per_step} of {len(all_rows)} query rows per step (fp64 oracle)"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{per_step} query rows per step, cycling over all rows"},
@@ -414,10 +419,12 @@ class ConfigRun:
     rotation of calls (plain, and with an event pair around every
     partial-attention kernel)."""
 
-    def __init__(self, va, wl, name, dev, stream, path="auto"):
+    def __init__(self, va, wl, name, dev, stream, path="auto", kv_dtype=None, T=None, Hq=None):
         import torch
         self.va, self.wl, self.name, self.stream = va, wl, name, stream
-        self.w = w = wl.config_workload(name)
+        self.w = w = wl.config_workload(name, kv_dtype, T, Hq)
+        self.label = wl.variant_name(name, kv_dtype, T, Hq)
+        self.description = wl.describe(name, kv_dtype, T, Hq)
         self.nbytes = wl.algorithmic_bytes(w)
         self.kv_bytes = self.nbytes - 2 * w["q"].size * 2
         self.copies = 1 if self.kv_bytes > 4 * L2_BYTES else int(math.ceil(4 * L2_BYTES / self.kv_bytes))
@@ -513,7 +520,7 @@ def config_record(run, peak, launch_bound_bytes=8e6):
     tighter than the call) the partial kernel's own time and roofline
     fraction.  Launch-bound configurations report microseconds per call only."""
     win = run.window_timing()
-    rec = {"workload": run.wl.CONFIGS[run.name].description, "algorithmic_bytes": run.nbytes,
+    rec = {"workload": run.description, "algorithmic_bytes": run.nbytes,
            "us_per_call": win["median_us"], "us_per_call_min": win["min_us"], "us_per_call_max": win["max_us"],
            "windows": win["windows"], "calls_per_window": win["calls_per_window"],
            "GB/s": run.nbytes / (win["median_us"] * 1e-6) / 1e9,
@@ -544,7 +551,8 @@ def run_ours(args):
 
     stream = torch.cuda.Stream(dev)
     peak, peak_src = peaks()
-    run = ConfigRun(va, wl, args.config, dev, stream, path=args.path)
+    run = ConfigRun(va, wl, args.config, dev, stream, path=args.path, kv_dtype=args.kv_dtype, T=args.T,
+                    Hq=args.Hq)
     w, d, plan, info, nbytes, copies = run.w, run.d, run.plan, run.info, run.nbytes, run.copies
     launches_per_step = 1 + (1 if info["num_split_groups"] > 0 else 0)
 
@@ -646,15 +654,19 @@ def run_ours(args):
 
     # every other named configuration, one after the other (figures only; the
     # headline above is args.config)
-    per_config = {args.config: head}
+    per_config = {run.label: head}
     if not args.no_per_config and world == 1:
         del d
-        for name in ("tiny", "mtp4", "batched", "maxctx", "lookup16"):
-            if name == args.config:
+        # the five configurations, then the longest one in the 4-bit and
+        # 2-bit caches
+        runs = [(n, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
+        runs += [("maxctx", "int4"), ("maxctx", "int2")]
+        for name, kv_dtype in runs:
+            if wl.variant_name(name, kv_dtype) == run.label:
                 continue
             torch.cuda.empty_cache()
-            r = ConfigRun(va, wl, name, dev, stream, path=args.path)
-            per_config[name] = config_record(r, peak)
+            r = ConfigRun(va, wl, name, dev, stream, path=args.path, kv_dtype=kv_dtype)
+            per_config[name if kv_dtype is None else f"{name}/{kv_dtype}"] = config_record(r, peak)
             r.close()
             del r
 
@@ -668,7 +680,7 @@ def run_ours(args):
     if partial_us:
         achieved = nbytes / (partial_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic_record(kernel, args.config), "kernel": kernel,
+                "traffic": traffic_record(kernel, run.label), "kernel": kernel,
                 "kernel_us": partial_us, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": nbytes}
     cpu = None
@@ -681,7 +693,7 @@ def run_ours(args):
         "us_per_call": ms_per_step * 1e3,
         "frac_of_peak_hbm": value / world / peak,
         "config": {
-            "workload": f"{args.config}: {wl.CONFIGS[args.config].description}",
+            "workload": f"{run.label}: {run.description}",
             "kv_dtype": w["kv_dtype"], "T": w["T"], "seq_lens_sum": int(w["seq_lens"].sum()),
             "num_seqs": int(len(w["seq_lens"])), "Hq": w["Hq"], "Hkv": w["Hkv"], "head_dim": w["D"],
             "algorithmic_bytes": nbytes,
