@@ -52,6 +52,10 @@
  * with fewer bits (symmetric absmax scale per token and kv head, codes
  * clamped to +-7 / +-1, decode = code * scale), so every cached format shares
  * one definition of decode().
+ * Alignment: k_pages and v_pages start on a 16-byte boundary; on the tensor-
+ * core path (the default) so do q, out and the scales; every other pointer
+ * is aligned to its element type.  A call that breaks this returns
+ * VA_ERR_INVALID_ARGUMENT before anything is launched.
  * Row r of a kv head's packed tile is verify token t = r / G, query head
  * h = g*G + r % G.
  *
@@ -108,7 +112,8 @@ typedef enum {
 
 /* Which partial-attention kernel a plan uses. */
 typedef enum {
-    VA_PATH_AUTO = 0,  /* tensor cores once the packed rows fill an MMA tile */
+    VA_PATH_AUTO = 0,  /* tensor cores (for every packed-row count; the CUDA-core
+                          kernel only if the tensor-core one does not fit) */
     VA_PATH_WARP = 1,  /* CUDA-core kernel: warp-shuffle reductions, any row count */
     VA_PATH_MMA = 2    /* tcgen05 tensor-core kernel (TMEM accumulators) */
 } va_path;
@@ -236,9 +241,11 @@ const char *verify_attn_last_cuda_error_string(void);
  * VA_ERR_SCRATCH_TOO_SMALL before anything touches the device.  Nothing is
  * allocated: no cudaMalloc, no cudaFree, no allocating library call.
  *
- * It always runs the CUDA-core partial kernel (the one a plan picks below 16
- * packed rows), also where a plan would pick the tensor-core kernel, so at
- * long contexts with many packed rows it is several times slower than
+ * It runs the partial kernel a plan picks (tensor cores) with the same one-
+ * wave split, made coarser while the partials do not fit; only a problem
+ * whose tensor-core partials cannot fit at any split of up to 16384 keys runs
+ * the CUDA-core kernel instead (unsplit if need be), which is several times
+ * slower at long contexts.  Pointer alignment is checked as for
  * verify_attn_with_plan.
  *
  * The first call on a device looks up the array's device address there
@@ -246,9 +253,8 @@ const char *verify_attn_last_cuda_error_string(void);
  * array, and each call overwrites what the previous one left there (its flag
  * word is cleared at the start of every call): calls that overlap on the GPU
  * race, so order them on one stream.  The work list is copied from static,
- * pageable host buffers with cudaMemcpyAsync on every call, so a call must
- * not be captured into a CUDA graph (a replay would not see later work
- * lists).  Asynchronous like verify_attn. */
+ * pageable host buffers with cudaMemcpyAsync on every call.  Asynchronous
+ * like verify_attn. */
 int verify_attn_noalloc(const int32_t *seq_lens_host, int num_seqs, int T,
                         int num_q_heads, int num_kv_heads, int head_dim,
                         va_kv_dtype kv_dtype, const void *q,

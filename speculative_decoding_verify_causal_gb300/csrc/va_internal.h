@@ -81,6 +81,12 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // Remember a failing CUDA call for verify_attn_last_cuda_error (thread-local).
 void note_cuda_error(cudaError_t e);
 
+// Whether the caller's pointers meet the alignment the partial kernel of
+// `path` (a va_path, WARP or MMA) and the combine rely on.
+bool aligned_for(int path, int kv_dtype, const void *q, const void *k_pages, const void *v_pages,
+                 const float *k_scale, const float *v_scale, const int32_t *block_table,
+                 const int32_t *seq_lens, const void *out, const float *lse);
+
 // Kernel launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_warp_partial(const PartialParams &p, int head_dim, int kv_dtype,
                                 int num_items, cudaStream_t s);
@@ -95,7 +101,6 @@ constexpr int kWarpRows = 16;    // packed rows per work item, CUDA-core kernel
 constexpr int kWarpTile = 32;    // keys per smem tile, CUDA-core kernel
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
 constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
-constexpr int kMmaMinRows = 16;  // packed rows from which the planner picks tcgen05
 constexpr int kMmaMaxItemTokens = 16384;  // longest split of the tcgen05 kernel (page ids in smem)
 constexpr size_t kMaxSmemPerBlock = 232448;  // opt-in dynamic shared memory per block (227 KB)
 

@@ -14,9 +14,10 @@
 // Every call shares the array and overwrites the previous call's contents;
 // the flag word is cleared at the start of each call and can be read back
 // with verify_attn_noalloc_flags.  The work list is staged in static host
-// buffers and copied with cudaMemcpyAsync from pageable memory, so a call is
-// not meant to be captured into a CUDA graph.  Only the CUDA-core partial
-// kernel runs here (for every packed-row count).
+// buffers and copied with cudaMemcpyAsync from pageable memory.  The partial
+// kernel is the one a plan picks (tensor cores), unless its split partials
+// cannot fit in the scratch at any split length its page-id staging allows:
+// then the CUDA-core kernel runs, with splits as coarse as needed.
 #include <cmath>
 #include <mutex>
 
@@ -149,35 +150,54 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
         return VA_ERR_INVALID_ARGUMENT;
     const int bt_stride = block_table_stride > 0 ? block_table_stride : max_pages;
 
-    // Geometry: the CUDA-core kernel's row groups and key tile, one wave of
-    // splits over the SMs (2 resident CTAs each), made coarser until the
-    // split partials fit in the scratch.  A problem that does not fit even
+    // Geometry: the tensor-core kernel's row groups and key tile with one
+    // wave of splits over the SMs (one resident CTA each), made coarser until
+    // the split partials fit in the scratch (at most kMmaMaxItemTokens keys
+    // per item); failing that, the CUDA-core kernel's (two CTAs per SM, no
+    // limit on the split).  A problem whose work list does not fit even
     // unsplit is rejected here, before any CUDA call.
     const int G = Hq / Hkv;
     const int R = G * T;
+    auto geometry = [&](bool mma, Layout &L) {
+        L = Layout{};
+        L.num_row_groups = (R + (mma ? va::kMmaRows : va::kWarpRows) - 1) / (mma ? va::kMmaRows : va::kWarpRows);
+        L.rows_per_group = (R + L.num_row_groups - 1) / L.num_row_groups;
+        L.tile = mma ? va::kMmaTile : va::kWarpTile;
+    };
+    const bool mma_fits_smem = va::mma_smem_bytes(D, kv_dtype, Hkv) <= va::kMaxSmemPerBlock;
     Layout L{};
-    L.num_row_groups = (R + va::kWarpRows - 1) / va::kWarpRows;
-    L.rows_per_group = (R + L.num_row_groups - 1) / L.num_row_groups;
-    L.tile = va::kWarpTile;
-    if (!layout_for(seq_lens_host, B, Hkv, D, max_len, L) || L.total > VA_NOALLOC_SCRATCH_BYTES)
-        return VA_ERR_SCRATCH_TOO_SMALL;
+    geometry(false, L);
+    const bool warp_possible = layout_for(seq_lens_host, B, Hkv, D, max_len, L) && L.total <= VA_NOALLOC_SCRATCH_BYTES;
+    bool mma_possible = false;
+    if (mma_fits_smem) {
+        geometry(true, L);
+        const int cap = max_len < va::kMmaMaxItemTokens ? max_len : va::kMmaMaxItemTokens;
+        mma_possible = layout_for(seq_lens_host, B, Hkv, D, cap, L) && L.total <= VA_NOALLOC_SCRATCH_BYTES;
+    }
+    if (!warp_possible && !mma_possible) return VA_ERR_SCRATCH_TOO_SMALL;
+    const bool mma = mma_possible;
+    if (!va::aligned_for(mma ? VA_PATH_MMA : VA_PATH_WARP, kv_dtype, q, k_pages, v_pages, k_scale, v_scale,
+                         block_table, seq_lens, out, lse))
+        return VA_ERR_INVALID_ARGUMENT;
 
     void *scratch = nullptr;
     int num_sms = 0;
     int rc = device_setup(&scratch, &num_sms);
     if (rc != VA_OK) return rc;
-    const long long slots = 2LL * num_sms;
-    long long c = (total_len + slots - 1) / slots;
+    geometry(mma, L);
+    const int cap = mma ? (max_len < va::kMmaMaxItemTokens ? max_len : va::kMmaMaxItemTokens) : max_len;
+    const long long slots = (mma ? 1LL : 2LL) * num_sms;
+    long long c = (total_len * Hkv * L.num_row_groups + slots - 1) / slots;
     c = (c + L.tile - 1) / L.tile * L.tile;
     if (c < 4 * L.tile) c = 4 * L.tile;
     bool fits = false;
     for (;;) {
-        const int split = c > max_len ? max_len : (int)c;
+        const int split = c > cap ? cap : (int)c;
         if (layout_for(seq_lens_host, B, Hkv, D, split, L) && L.total <= VA_NOALLOC_SCRATCH_BYTES) {
             fits = true;
             break;
         }
-        if (split >= max_len) break;  // already unsplit: the work list itself is too large
+        if (split >= cap) break;  // as coarse as this kernel allows (checked above: not reached)
         c *= 2;
     }
     if (!fits) return VA_ERR_SCRATCH_TOO_SMALL;
@@ -235,7 +255,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     pp.num_pages = num_pages;  // 0: block-table entries unchecked
     pp.num_parts = L.num_parts;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-    e = va::launch_warp_partial(pp, D, kv_dtype, ni, s);
+    e = mma ? va::launch_mma_partial(pp, D, kv_dtype, ni, s) : va::launch_warp_partial(pp, D, kv_dtype, ni, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (ng > 0) {
         va::CombineParams cp{};

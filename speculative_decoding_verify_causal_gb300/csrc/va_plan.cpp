@@ -105,12 +105,17 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
     return VA_OK;
 }
 
-// Tensor cores once the packed rows of a kv head (G * T) reach an MMA row
-// tile's worth of work; CUDA-core dot products below that.
+// Tensor cores for every packed-row count: even a single row (T = 1, G = 1)
+// padded to the 128-row MMA tile runs 2-12x faster than the CUDA-core kernel
+// on GB300, from 256 to 262k cached tokens (measured for T in 1..3 and G in
+// 1..15 at D = 128 / 256), because the tile's cost is the KV stream, not the
+// padded rows.  The CUDA-core kernel remains for an explicit request and for
+// a tensor-core configuration that does not fit in shared memory.
 int choose_path(int R, int Hkv, const va_plan_options *opts) {
+    (void)R;
+    (void)Hkv;
     int want = opts ? opts->path : VA_PATH_AUTO;
-    if (want != VA_PATH_AUTO) return want;
-    return R >= va::kMmaMinRows ? VA_PATH_MMA : VA_PATH_WARP;
+    return want != VA_PATH_AUTO ? want : VA_PATH_MMA;
 }
 
 int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int dtype,
@@ -273,6 +278,22 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 namespace va {
 void note_cuda_error(cudaError_t e) {
     if (e != cudaSuccess) t_last_cuda_error = (int)e;
+}
+
+bool aligned_for(int path, int kv_dtype, const void *q, const void *k_pages, const void *v_pages,
+                 const float *k_scale, const float *v_scale, const int32_t *block_table,
+                 const int32_t *seq_lens, const void *out, const float *lse) {
+    auto ok = [](const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; };
+    const bool quant = kv_dtype != VA_BF16;
+    // cache rows move in 16-byte units in both kernels (TMA boxes, or
+    // 16 / 8 / 4-byte vector loads at 16-byte aligned row offsets)
+    if (!ok(k_pages, 16) || !ok(v_pages, 16)) return false;
+    if (!ok(q, 2) || !ok(out, 2) || !ok(block_table, 4) || !ok(seq_lens, 4) || (lse && !ok(lse, 4))) return false;
+    if (quant && (!ok(k_scale, 4) || !ok(v_scale, 4))) return false;
+    // the tensor-core kernel moves q, out and the scales in 16-byte units too
+    if (path == VA_PATH_MMA && (!ok(q, 16) || !ok(out, 16) || (quant && (!ok(k_scale, 16) || !ok(v_scale, 16)))))
+        return false;
+    return true;
 }
 }  // namespace va
 
@@ -491,13 +512,9 @@ int verify_attn_with_plan(const va_plan *p, const void *q, const void *k_pages,
     pp.num_parts = p->num_parts;
     pp.sm_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->D));
 
-    if (p->path == VA_PATH_MMA) {
-        // TMA and bulk copies need 16-byte aligned bases
-        auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
-        if (misaligned(k_pages) || misaligned(v_pages) || misaligned(q) || misaligned(out) ||
-            (p->kv_dtype != VA_BF16 && (misaligned(k_scale) || misaligned(v_scale))))
-            return VA_ERR_INVALID_ARGUMENT;
-    }
+    if (!va::aligned_for(p->path, p->kv_dtype, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,
+                         out, lse))
+        return VA_ERR_INVALID_ARGUMENT;
     if (p->ev_before && cudaEventRecordWithFlags(p->ev_before, s, cudaEventRecordExternal) != cudaSuccess)
         return VA_ERR_CUDA;
     cudaError_t e = p->path == VA_PATH_MMA

@@ -97,11 +97,16 @@ def test_planner_fills_the_chip_for_one_long_sequence():
     assert info["max_splits"] > 1
 
 
-def test_planner_picks_tensor_cores_from_an_mma_tile_of_rows():
-    # G*T >= 16 packed rows -> tcgen05 kernel; fewer -> CUDA-core kernel
+def test_planner_picks_tensor_cores_for_every_row_count():
+    # the tcgen05 kernel by default, down to a single packed row (measured
+    # faster than the CUDA-core kernel at every row count and context length);
+    # the CUDA-core kernel only on request
     big, _ = va.verify_attn_plan_describe([25016], 16, 24, 4, 256, "int8", num_sms=148)
     small, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148)
-    assert big["path"] == 2 and small["path"] == 1
+    one, _ = va.verify_attn_plan_describe([261], 1, 1, 1, 64, "bf16", num_sms=148)
+    forced, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148, path="warp")
+    assert big["path"] == 2 and small["path"] == 2 and one["path"] == 2 and forced["path"] == 1
+    assert small["rows_per_group"] == 2 and small["num_row_groups"] == 1
     assert big["rows_per_group"] == 96 and big["num_row_groups"] == 1
     # one CTA per SM for the tensor-core kernel: about one wave of items
     assert 148 * 0.75 <= big["num_items"] <= 148

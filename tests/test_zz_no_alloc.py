@@ -66,6 +66,7 @@ def test_noalloc_matches_oracle_and_planned_entry_on_two_calls_in_a_row():
     cases = [
         wl.make_workload(301, [2500, 40, 777], 5, 24, 4, 256, "fp8_e4m3"),   # split + unsplit rows
         wl.make_workload(302, [25016], 16, 24, 4, 256, "int8"),             # long context, many splits
+        wl.make_workload(303, [9001, 123], 1, 8, 4, 128, "int4"),           # two packed rows, 4-bit cache
     ]
     for i, w in enumerate(cases):
         d = wl.to_device(w)
