@@ -97,8 +97,9 @@ cudaError_t launch_mma_partial(const PartialParams &p, int head_dim, int kv_dtyp
 size_t mma_smem_bytes(int head_dim, int kv_dtype, int num_kv_heads);
 
 // Geometry of each path.
-constexpr int kWarpRows = 16;    // packed rows per work item, CUDA-core kernel
-constexpr int kWarpTile = 32;    // keys per smem tile, CUDA-core kernel
+constexpr int kWarpRows = 4;     // packed rows per work item, CUDA-core kernel
+constexpr int kWarpTile = 32;    // split granularity (keys), CUDA-core kernel
+constexpr int kWarpCtasPerSm = 3;  // resident CTAs of the CUDA-core kernel per SM
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
 constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
 constexpr int kMmaMaxItemTokens = 16384;  // longest split of the tcgen05 kernel (page ids in smem)

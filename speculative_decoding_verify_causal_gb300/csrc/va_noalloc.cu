@@ -153,7 +153,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     // Geometry: the tensor-core kernel's row groups and key tile with one
     // wave of splits over the SMs (one resident CTA each), made coarser until
     // the split partials fit in the scratch (at most kMmaMaxItemTokens keys
-    // per item); failing that, the CUDA-core kernel's (two CTAs per SM, no
+    // per item); failing that, the CUDA-core kernel's (several CTAs per SM, no
     // limit on the split).  A problem whose work list does not fit even
     // unsplit is rejected here, before any CUDA call.
     const int G = Hq / Hkv;
@@ -186,7 +186,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     if (rc != VA_OK) return rc;
     geometry(mma, L);
     const int cap = mma ? (max_len < va::kMmaMaxItemTokens ? max_len : va::kMmaMaxItemTokens) : max_len;
-    const long long slots = (mma ? 1LL : 2LL) * num_sms;
+    const long long slots = (long long)(mma ? 1 : va::kWarpCtasPerSm) * num_sms;
     long long c = (total_len * Hkv * L.num_row_groups + slots - 1) / slots;
     c = (c + L.tile - 1) / L.tile * L.tile;
     if (c < 4 * L.tile) c = 4 * L.tile;

@@ -1,27 +1,39 @@
-// CUDA-core partial-attention kernel (the small-row path).
+// CUDA-core partial-attention kernel: the few-rows path.
 //
-// Used when the packed rows of a kv head (G query heads x T verify tokens)
-// are too few to fill a tensor-core tile, e.g. T = 1 decode with a small
-// group, and as the always-available fallback.  Dot products run on the
-// FP32 pipes with warp-shuffle reductions for the softmax statistics.
+// For a kv head whose packed rows (G query heads x T verify tokens) are too
+// few to fill a tensor-core tile -- T = 1 decode with a small group -- the
+// dot products run on the FP32 pipes ("I pushed Qwen3.8-27B to 124 tps on a
+// single request on a RTX 3090", bullet "Split-KV attention kernel for the
+// verify step": split the cache so that a handful of queries still fills the
+// chip).  Each CTA takes one work item: up to 4 packed rows of one kv head of
+// one sequence over one key range.  Nothing is staged in shared memory on the
+// way: every warp streams its own batches of keys straight into registers and
+// keeps its own online-softmax state, and the CTA's four warps merge their
+// states once at the end.
 //
-// One CTA = one work item: up to 16 packed rows of one kv head of one
-// sequence over one key range (one split of "split-KV", from "I pushed
-// Qwen3.8-27B to 124 tps on a single request on a RTX 3090", bullet
-// "Split-KV attention kernel for the verify step").  Per 32-key tile:
-//   1. the 32 K and V rows are gathered through the block table (16-byte
-//      loads; 8 / 4 bytes for the 4-bit / 2-bit caches), dequantised
-//      (fp8-e4m3 / int8 / int4 / int2 times the per-token scale, or bf16) and
-//      staged in shared memory as fp32;
-//   2. lane j of each warp scores key j against the warp's rows, applies the
-//      bottom-right causal mask (verify token t sees keys j <= L - T + t) and
-//      updates the row's running max / sum with shuffles (online softmax in
-//      base 2: the scale log2(e)/sqrt(D) is folded into q);
-//   3. every thread owns a slice of head_dim for all rows and accumulates
-//      P x V after rescaling by exp2(m_old - m_new).
-// The item then writes either the final bf16 output and natural-log LSE (an
-// unsplit sequence) or its normalised fp32 partial and LSE for the combine.
+// Per batch of KG keys (a 16-token page holds one or two batches):
+//   * lane l owns elements [l D/32, (l+1) D/32) of every cache row, so the
+//     32 lanes read a row as one contiguous, coalesced run of D * bits / 8
+//     bytes (16 to 512), for the KG key rows and the KG value rows at once;
+//   * the codes become fp32 exactly on the FP32 pipe (integers through the
+//     2^23 magic number, bf16 by a shift; fp8-e4m3 through the hardware's
+//     exact conversion to fp16); the per-token scales multiply the scores and
+//     the probabilities, not the elements;
+//   * each lane's partial dot products of the batch (one per key and row) are
+//     summed across the warp by a transpose-reduction: at each of log2(KG)
+//     exchange steps a lane keeps half of its values and adds the partner's
+//     copy of them, so that after the plain steps that remain, lane l holds
+//     the full score of key key_of(l) -- about one shuffle per key and row;
+//   * base-2 online softmax with the running max moved (and the accumulator
+//     rescaled) only when a batch's max exceeds it by more than 2^8; the
+//     probabilities times the v scale are broadcast back by shuffles and
+//     accumulated into each lane's slice of O.
+// Rows past the item's count and keys past its end or the causal bound
+// (verify token t sees keys j <= L - T + t) weigh zero.  The item writes the
+// final bf16 output and natural-log LSE (an unsplit sequence) or its
+// normalised fp32 partial and LSE for the combine.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -30,10 +42,91 @@
 namespace va {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleLog2 = 8.0f;
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+__host__ __device__ constexpr int elem_bits(int dt) {
+    return dt == VA_BF16 ? 16 : dt == VA_INT4 ? 4 : dt == VA_INT2 ? 2 : 8;
+}
+
+// A lane's slice of one cache row: LB = (D / 32) * bits bits, loaded as the
+// narrowest aligned unit that holds it.  Slices of 4 bits (2-bit codes at
+// D = 64) share a byte between two lanes.
+template <int LB>
+struct Slice {
+    static constexpr int kWords = LB >= 32 ? LB / 32 : 1;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(const uint8_t *row, int lane) {
+        if constexpr (LB == 128) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row) + lane);
+            w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+        } else if constexpr (LB == 64) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row) + lane);
+            w[0] = v.x, w[1] = v.y;
+        } else if constexpr (LB == 32) {
+            w[0] = __ldg(reinterpret_cast<const uint32_t *>(row) + lane);
+        } else if constexpr (LB == 16) {
+            w[0] = __ldg(reinterpret_cast<const uint16_t *>(row) + lane);
+        } else if constexpr (LB == 8) {
+            w[0] = __ldg(row + lane);
+        } else {
+            static_assert(LB == 4, "slice width");
+            w[0] = (uint32_t)__ldg(row + (lane >> 1)) >> (4 * (lane & 1));
+        }
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) w[i] = 0u;
+    }
+};
+
+// The slice's EL codes as exact fp32 values (the code, not yet scaled).
+// Integers: a code c with offset u = c + 2^(b-1) in [0, 2^b) is placed in the
+// low mantissa bits of 2^23 (u XOR-ed into 0x4B000000 | 2^(b-1) flips the
+// sign bit of the two's-complement field into that offset), and 2^23 plus
+// the offset is subtracted: both steps are exact.
+template <int DT, int EL>
+__device__ __forceinline__ void decode(const uint32_t *w, float *f) {
+    if constexpr (DT == VA_BF16) {
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+            const uint32_t x = w[e / 2];
+            f[e] = __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
+        }
+    } else if constexpr (DT == VA_INT8) {
+#pragma unroll
+        for (int i = 0; i < (EL + 3) / 4; ++i) {
+            const uint32_t x = w[i] ^ 0x80808080u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (4 * i + k < EL)
+                    f[4 * i + k] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440 + k)) - 8388736.0f;
+        }
+    } else if constexpr (DT == VA_INT4) {
+#pragma unroll
+        for (int e = 0; e < EL; ++e)
+            f[e] = __uint_as_float(((w[e / 8] >> (4 * (e % 8))) & 0xFu) ^ 0x4B000008u) - 8388616.0f;
+    } else if constexpr (DT == VA_INT2) {
+#pragma unroll
+        for (int e = 0; e < EL; ++e)
+            f[e] = __uint_as_float(((w[e / 16] >> (2 * (e % 16))) & 0x3u) ^ 0x4B000002u) - 8388610.0f;
+    } else {  // fp8-e4m3
+#pragma unroll
+        for (int i = 0; i < (EL + 1) / 2; ++i) {
+            const uint32_t x = w[i / 2] >> (16 * (i % 2));
+            __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xFFFFu), __NV_E4M3);
+            const float2 v = __half22float2(*reinterpret_cast<__half2 *>(&h));
+            f[2 * i] = v.x;
+            if (2 * i + 1 < EL) f[2 * i + 1] = v.y;
+        }
+    }
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
@@ -41,305 +134,275 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
-// Decode the 16 bytes of `raw` (one aligned chunk of a cache row) into floats.
-template <int DT>
-__device__ __forceinline__ void decode16(const uint4 &raw, float *dst, float scale);
+template <int KG>
+struct KeyBits {
+    static constexpr int value = KG == 16 ? 4 : KG == 8 ? 3 : KG == 4 ? 2 : 1;
+};
 
-template <>
-__device__ __forceinline__ void decode16<VA_BF16>(const uint4 &raw, float *dst, float) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+// Transpose-reduction of KG values per lane over the warp: afterwards every
+// lane's v[0] is the warp-wide sum of value key_of_lane(lane), whose bits are
+// lane bits 4, 3, ... (most significant first, log2(KG) of them).
+template <int KG>
+__device__ __forceinline__ void transpose_reduce(float (&v)[KG], int lane) {
+    constexpr int kB = KeyBits<KG>::value;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        dst[2 * i] = __uint_as_float(w[i] << 16);
-        dst[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
-template <>
-__device__ __forceinline__ void decode16<VA_FP8_E4M3>(const uint4 &raw, float *dst, float scale) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        if (step < kB) {
+            const int half = KG >> (step + 1);
+            const bool upper = (lane & o) != 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-            __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hlf));
-            __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            float2 f = __half22float2(*reinterpret_cast<__half2 *>(&h2));
-            dst[4 * i + 2 * hlf] = f.x * scale;
-            dst[4 * i + 2 * hlf + 1] = f.y * scale;
+            for (int i = 0; i < KG / 2; ++i) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
         }
     }
 }
 
-template <>
-__device__ __forceinline__ void decode16<VA_INT8>(const uint4 &raw, float *dst, float scale) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            dst[4 * i + k] = static_cast<float>(static_cast<int8_t>(w[i] >> (8 * k))) * scale;
+template <int KG>
+__device__ __forceinline__ int key_of_lane(int lane) {
+    return (lane >> (5 - KeyBits<KG>::value)) & (KG - 1);
 }
 
-// 4-bit / 2-bit caches: 16 codes in 8 / 4 bytes (raw.x, raw.y), code k of a
-// word in bits [k bits, (k + 1) bits), sign-extended by an arithmetic shift.
-template <>
-__device__ __forceinline__ void decode16<VA_INT4>(const uint4 &raw, float *dst, float scale) {
-    const uint32_t w[2] = {raw.x, raw.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            dst[8 * i + k] = static_cast<float>(static_cast<int32_t>(w[i] << (28 - 4 * k)) >> 28) * scale;
+template <int KG>
+__device__ __forceinline__ int lane_of_key(int k) {
+    return k << (5 - KeyBits<KG>::value);
 }
 
-template <>
-__device__ __forceinline__ void decode16<VA_INT2>(const uint4 &raw, float *dst, float scale) {
+// Maximum over the batch's keys (the lanes of one key hold the same value).
+template <int KG>
+__device__ __forceinline__ float key_max(float v) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-        dst[k] = static_cast<float>(static_cast<int32_t>(raw.x << (30 - 2 * k)) >> 30) * scale;
-}
-
-// Bits per cached element, and the raw bytes holding one decode16 chunk.
-template <int DT>
-__host__ __device__ constexpr int elem_bits() {
-    return DT == VA_BF16 ? 16 : DT == VA_INT4 ? 4 : DT == VA_INT2 ? 2 : 8;
-}
-
-// One chunk of a cache row as 16 / 8 / 4 aligned bytes (unused words zero).
-template <int BYTES>
-__device__ __forceinline__ uint4 load_chunk(const uint8_t *src) {
-    if constexpr (BYTES == 16) {
-        return *reinterpret_cast<const uint4 *>(src);
-    } else if constexpr (BYTES == 8) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
-        return make_uint4(v.x, v.y, 0u, 0u);
-    } else {
-        return make_uint4(*reinterpret_cast<const uint32_t *>(src), 0u, 0u, 0u);
-    }
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int i = 0; i < KeyBits<KG>::value; ++i) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16 >> i));
     return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+template <int D, int DT, int RPI>
+struct Geometry {
+    static constexpr int EL = D / 32;                   // elements of a row per lane
+    static constexpr int LB = EL * elem_bits(DT);       // bits of a row per lane
+    static constexpr int ROWB = D * elem_bits(DT) / 8;  // bytes per cache row
+    static constexpr int KG = RPI == 1 ? 16 : 8;        // keys per batch
+};
 
-template <int D>
-constexpr int smem_floats() {
-    return kWarpRows * D + kWarpTile * (D + 1) + kWarpTile * D + kWarpRows * kWarpTile +
-           3 * kWarpRows + kWarpTile;
-}
+template <int D, int DT, int RPI>
+__global__ void __launch_bounds__(kThreads, kWarpCtasPerSm) warp_partial_kernel(const PartialParams p) {
+    using Gm = Geometry<D, DT, RPI>;
+    constexpr int EL = Gm::EL, KG = Gm::KG;
+    constexpr bool kQuant = DT != VA_BF16;
+    static_assert(VA_PAGE_SIZE % KG == 0 && kWarpTile % KG == 0, "a batch lies inside one page");
+    __shared__ float sm_m[kWarps][RPI], sm_l[kWarps][RPI];
+    __shared__ float sm_o[kWarps][RPI][D];
 
-template <int D, int DT>
-__global__ void __launch_bounds__(kThreads) warp_partial_kernel(const PartialParams p) {
-    constexpr int RB = kWarpRows;
-    constexpr int TK = kWarpTile;
-    constexpr int EPC = DT == VA_BF16 ? 8 : 16;     // elements per decoded chunk
-    constexpr int CB = EPC * elem_bits<DT>() / 8;   // raw bytes per chunk (16, 8 or 4)
-    constexpr int RB_BYTES = D * elem_bits<DT>() / 8;  // bytes per cache row
-    constexpr int CPR = D / EPC;                    // chunks per cache row
-    constexpr int DPT = (D + kThreads - 1) / kThreads;  // head_dim slice per thread
     // programmatic dependent launch: nothing of the caller's is touched before this
     griddep_wait();
-
-    extern __shared__ float smem[];
-    float *Qs = smem;                 // [RB][D]   q * log2(e)/sqrt(D)
-    float *Ks = Qs + RB * D;          // [TK][D+1] dequantised keys (padded rows)
-    float *Vs = Ks + TK * (D + 1);    // [TK][D]   dequantised values
-    float *Ps = Vs + TK * D;          // [RB][TK]  probabilities of the tile
-    float *As = Ps + RB * TK;         // [RB]      rescale factor of the tile
-    float *Ms = As + RB;              // [RB]      final running max (log2 units)
-    float *Ls = Ms + RB;              // [RB]      final running sum
-    int *Valid = reinterpret_cast<int *>(Ls + RB);  // [TK] key passed bound checks
-
     const Item it = p.items[blockIdx.x];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = p.G, T = p.T;
+    const int G = p.G, T = p.T, Hkv = p.Hkv;
     const int row0 = it.rg * p.rows_per_group;
     const int nrows = min(p.rows_per_group, p.R - row0);
-    const int Hkv = p.Hkv;
-
     if (tid == 0 && p.seq_lens[it.b] != it.L) atomicOr(p.flags, kFlagSeqLenMismatch);
 
-    for (int i = tid; i < RB * D; i += kThreads) {
-        const int r = i / D, d = i % D;
-        float v = 0.f;
+    // this lane's slice of the item's q rows, times log2(e) / sqrt(D)
+    float q[RPI][EL];
+    int last_visible[RPI];
+#pragma unroll
+    for (int r = 0; r < RPI; ++r) {
+        last_visible[r] = -1;  // padding rows see nothing
+#pragma unroll
+        for (int e = 0; e < EL; ++e) q[r][e] = 0.f;
         if (r < nrows) {
             const int rr = row0 + r;
             const int t = rr / G, h = it.kvh * G + rr % G;
-            v = bf16_bits_to_float(p.q[((size_t)(it.b * T + t) * p.Hq + h) * D + d]) * p.sm_scale_log2;
+            const uint16_t *qrow = p.q + ((size_t)(it.b * T + t) * p.Hq + h) * D + lane * EL;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) q[r][e] = __uint_as_float((uint32_t)__ldg(qrow + e) << 16) * p.sm_scale_log2;
+            last_visible[r] = it.L - T + t;
         }
-        Qs[i] = v;
     }
 
-    float m_run[RB / 4], l_run[RB / 4];
+    float m_run[RPI], l_run[RPI], acc[RPI][EL];
 #pragma unroll
-    for (int i = 0; i < RB / 4; ++i) {
-        m_run[i] = -INFINITY;
-        l_run[i] = 0.f;
+    for (int r = 0; r < RPI; ++r) {
+        m_run[r] = -INFINITY;
+        l_run[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
     }
-    float acc[RB][DPT];
-#pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-        for (int k = 0; k < DPT; ++k) acc[r][k] = 0.f;
 
     const uint8_t *kbase = static_cast<const uint8_t *>(p.k_pages);
     const uint8_t *vbase = static_cast<const uint8_t *>(p.v_pages);
     const int32_t *bt = p.block_table + (size_t)it.b * p.bt_stride;
+    const int my_key = key_of_lane<KG>(lane);
+    const bool key_owner = (lane & ((32 / KG) - 1)) == 0;  // one lane per key adds to l
+    const int nbatch = (it.k_end - it.k_begin + KG - 1) / KG;
 
-    for (int k0 = it.k_begin; k0 < it.k_end; k0 += TK) {
-        __syncthreads();  // previous tile fully consumed
-        if (tid < TK) {
-            const int key = k0 + tid;
-            int ok = key < it.k_end;
-            if (ok && p.num_pages > 0) {
-                const int page = bt[key / VA_PAGE_SIZE];
-                if (page < 0 || page >= p.num_pages) {
-                    atomicOr(p.flags, kFlagBadPage);
-                    ok = 0;
+    // Batches are dealt to the warps round-robin; every batch lies inside one
+    // 16-token page (items start at multiples of the 32-key split tile).
+    for (int bi = warp; bi < nbatch; bi += kWarps) {
+        const int j0 = it.k_begin + bi * KG;
+        int page = __ldg(bt + j0 / VA_PAGE_SIZE);
+        bool page_ok = true;
+        if (p.num_pages > 0 && (page < 0 || page >= p.num_pages)) {
+            if (lane == 0) atomicOr(p.flags, kFlagBadPage);
+            page_ok = false;
+            page = 0;  // not read: the batch's keys are all masked below
+        }
+        const size_t row_first = ((size_t)page * VA_PAGE_SIZE + j0 % VA_PAGE_SIZE) * Hkv + it.kvh;
+        const int nvalid = page_ok ? min(KG, it.k_end - j0) : 0;
+
+        // every load of the batch first: KG key slices, KG value slices, the
+        // scales of this lane's key
+        Slice<Gm::LB> k_raw[KG], v_raw[KG];
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            if (k < nvalid) {
+                const size_t row = row_first + (size_t)k * Hkv;
+                k_raw[k].load(kbase + row * Gm::ROWB, lane);
+                v_raw[k].load(vbase + row * Gm::ROWB, lane);
+            } else {
+                k_raw[k].zero();
+                v_raw[k].zero();
+            }
+        }
+        float kscale = 1.f, vscale = 1.f;
+        if (kQuant && my_key < nvalid) {
+            const size_t row = row_first + (size_t)my_key * Hkv;
+            kscale = __ldg(p.k_scale + row);
+            vscale = __ldg(p.v_scale + row);
+        }
+
+        // scores: this lane's partial dot products, then the transpose-reduction
+        float s[RPI];
+        {
+            float part[RPI][KG];
+#pragma unroll
+            for (int k = 0; k < KG; ++k) {
+                float f[EL];
+                decode<DT, EL>(k_raw[k].w, f);
+#pragma unroll
+                for (int r = 0; r < RPI; ++r) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) a = fmaf(q[r][e], f[e], a);
+                    part[r][k] = a;
                 }
             }
-            Valid[tid] = ok;
-        }
-        __syncthreads();
-        for (int c = tid; c < TK * CPR; c += kThreads) {
-            const int j = c / CPR, part = c % CPR;
-            const int key = k0 + j;
-            float kf[EPC], vf[EPC];
-            if (Valid[j]) {
-                const int page = bt[key / VA_PAGE_SIZE];
-                const size_t row = ((size_t)page * VA_PAGE_SIZE + key % VA_PAGE_SIZE) * Hkv + it.kvh;
-                const uint4 kr = load_chunk<CB>(kbase + row * RB_BYTES + part * CB);
-                const uint4 vr = load_chunk<CB>(vbase + row * RB_BYTES + part * CB);
-                const float ks = DT == VA_BF16 ? 1.f : p.k_scale[row];
-                const float vs = DT == VA_BF16 ? 1.f : p.v_scale[row];
-                decode16<DT>(kr, kf, ks);
-                decode16<DT>(vr, vf, vs);
-            } else {
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) kf[e] = vf[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) {
-                Ks[j * (D + 1) + part * EPC + e] = kf[e];
-                Vs[j * D + part * EPC + e] = vf[e];
+            for (int r = 0; r < RPI; ++r) {
+                transpose_reduce<KG>(part[r], lane);
+                const bool vis = my_key < nvalid && j0 + my_key <= last_visible[r];
+                s[r] = vis ? part[r][0] * kscale : -INFINITY;
             }
         }
-        __syncthreads();
 
-        // scores + online softmax statistics: warp w owns rows w, w+4, ...
+        // online softmax per row, then P x V into this lane's slice of O
+        float pv[RPI];
 #pragma unroll
-        for (int i = 0; i < RB / 4; ++i) {
-            const int r = warp + 4 * i;
-            if (r >= nrows) break;
-            const int t = (row0 + r) / G;
-            const int key = k0 + lane;
-            const bool vis = Valid[lane] && key <= it.L - T + t;
-            float dot = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < D; ++d) dot = fmaf(Qs[r * D + d], Ks[lane * (D + 1) + d], dot);
-            const float s = vis ? dot : -INFINITY;
-            const float m_new = fmaxf(m_run[i], warp_max(s));
-            float alpha = 1.f, pr = 0.f;
-            if (m_new != -INFINITY) {
-                alpha = m_run[i] == -INFINITY ? 0.f : exp2f(m_run[i] - m_new);
-                pr = vis ? exp2f(s - m_new) : 0.f;
+        for (int r = 0; r < RPI; ++r) {
+            const float bmax = key_max<KG>(s[r]);
+            if (bmax > m_run[r] + kRescaleLog2) {  // uniform across the warp
+                const float alpha = m_run[r] == -INFINITY ? 0.f : ex2_approx(m_run[r] - bmax);
+                m_run[r] = bmax;
+                l_run[r] *= alpha;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) acc[r][e] *= alpha;
             }
-            l_run[i] = l_run[i] * alpha + warp_sum(pr);
-            m_run[i] = m_new;
-            Ps[r * TK + lane] = pr;
-            if (lane == 0) As[r] = alpha;
+            const float pr = s[r] == -INFINITY ? 0.f : ex2_approx(s[r] - m_run[r]);
+            if (key_owner) l_run[r] += pr;
+            pv[r] = pr * vscale;
         }
-        __syncthreads();
-
-        // P x V: thread owns columns d = tid + 128*k of every row
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            if (r < nrows) {
-                const float a = As[r];
+        for (int k = 0; k < KG; ++k) {
+            float f[EL];
+            decode<DT, EL>(v_raw[k].w, f);
 #pragma unroll
-                for (int k = 0; k < DPT; ++k) acc[r][k] *= a;
-            }
-        }
-        for (int j = 0; j < TK; ++j) {
-            float v[DPT];
+            for (int r = 0; r < RPI; ++r) {
+                const float w = __shfl_sync(0xffffffffu, pv[r], lane_of_key<KG>(k));
 #pragma unroll
-            for (int k = 0; k < DPT; ++k) {
-                const int d = tid + k * kThreads;
-                v[k] = d < D ? Vs[j * D + d] : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                const float pr = Ps[r * TK + j];
-#pragma unroll
-                for (int k = 0; k < DPT; ++k) acc[r][k] = fmaf(pr, v[k], acc[r][k]);
+                for (int e = 0; e < EL; ++e) acc[r][e] = fmaf(w, f[e], acc[r][e]);
             }
         }
     }
 
+    // merge the four warps' states: O = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w
 #pragma unroll
-    for (int i = 0; i < RB / 4; ++i) {
-        const int r = warp + 4 * i;
-        if (r < nrows && lane == 0) {
-            Ms[r] = m_run[i];
-            Ls[r] = l_run[i];
+    for (int r = 0; r < RPI; ++r) {
+        float l = l_run[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            sm_m[warp][r] = m_run[r];
+            sm_l[warp][r] = l;
         }
+#pragma unroll
+        for (int e = 0; e < EL; ++e) sm_o[warp][r][lane * EL + e] = acc[r][e];
     }
     __syncthreads();
-
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
+    for (int r = 0; r < RPI; ++r) {
         if (r >= nrows) break;
-        const float l = Ls[r];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float lse_nat = l > 0.f ? (Ms[r] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][r]);
+        float wgt[kWarps], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            wgt[w] = sm_m[w][r] == -INFINITY ? 0.f : exp2f(sm_m[w][r] - M);
+            L += wgt[w] * sm_l[w][r];
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float lse_nat = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
         const int rr = row0 + r;
         const int t = rr / G, h = it.kvh * G + rr % G;
-        if (it.part < 0) {
-            const size_t orow = ((size_t)(it.b * T + t) * p.Hq + h);
+        const size_t orow = (size_t)(it.b * T + t) * p.Hq + h;
+        const size_t prow = (size_t)it.part * p.rows_per_group + r;
+        for (int d = tid; d < D; d += kThreads) {
+            float o = 0.f;
 #pragma unroll
-            for (int k = 0; k < DPT; ++k) {
-                const int d = tid + k * kThreads;
-                if (d < D) p.out[orow * D + d] = float_to_bf16_bits(acc[r][k] * inv);
+            for (int w = 0; w < kWarps; ++w) o = fmaf(wgt[w], sm_o[w][r][d], o);
+            o *= inv;
+            if (it.part < 0)
+                p.out[orow * D + d] = float_to_bf16_bits(o);
+            else
+                p.o_part[prow * D + d] = o;
+        }
+        if (tid == 0) {
+            if (it.part < 0) {
+                if (p.lse) p.lse[orow] = lse_nat;
+            } else {
+                p.lse_part[prow] = lse_nat;
             }
-            if (tid == 0 && p.lse) p.lse[orow] = lse_nat;
-        } else {
-            const size_t prow = (size_t)it.part * p.rows_per_group + r;
-#pragma unroll
-            for (int k = 0; k < DPT; ++k) {
-                const int d = tid + k * kThreads;
-                if (d < D) p.o_part[prow * D + d] = acc[r][k] * inv;
-            }
-            if (tid == 0) p.lse_part[prow] = lse_nat;
         }
     }
 }
 
-template <int D, int DT>
+template <int D, int DT, int RPI>
 cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
-    const size_t smem = sizeof(float) * smem_floats<D>();
-    auto k = warp_partial_kernel<D, DT>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(n), dim3(kThreads), smem, s, p);
+    return launch_pdl(warp_partial_kernel<D, DT, RPI>, dim3(n), dim3(kThreads), 0, s, p);
+}
+
+template <int D, int DT>
+cudaError_t launch_rows(const PartialParams &p, int n, cudaStream_t s) {
+    if (p.rows_per_group <= 1) return launch_one<D, DT, 1>(p, n, s);
+    if (p.rows_per_group <= 2) return launch_one<D, DT, 2>(p, n, s);
+    return launch_one<D, DT, 4>(p, n, s);
 }
 
 template <int D>
 cudaError_t launch_d(const PartialParams &p, int dtype, int n, cudaStream_t s) {
     switch (dtype) {
-    case VA_BF16: return launch_one<D, VA_BF16>(p, n, s);
-    case VA_FP8_E4M3: return launch_one<D, VA_FP8_E4M3>(p, n, s);
-    case VA_INT8: return launch_one<D, VA_INT8>(p, n, s);
-    case VA_INT4: return launch_one<D, VA_INT4>(p, n, s);
-    default: return launch_one<D, VA_INT2>(p, n, s);
+    case VA_BF16: return launch_rows<D, VA_BF16>(p, n, s);
+    case VA_FP8_E4M3: return launch_rows<D, VA_FP8_E4M3>(p, n, s);
+    case VA_INT8: return launch_rows<D, VA_INT8>(p, n, s);
+    case VA_INT4: return launch_rows<D, VA_INT4>(p, n, s);
+    default: return launch_rows<D, VA_INT2>(p, n, s);
     }
 }
 
@@ -348,6 +411,7 @@ cudaError_t launch_d(const PartialParams &p, int dtype, int n, cudaStream_t s) {
 cudaError_t launch_warp_partial(const PartialParams &p, int head_dim, int kv_dtype, int n,
                                 cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
+    if (p.rows_per_group > kWarpRows) return cudaErrorInvalidValue;
     switch (head_dim) {
     case 64: return launch_d<64>(p, kv_dtype, n, s);
     case 128: return launch_d<128>(p, kv_dtype, n, s);
