@@ -665,15 +665,17 @@ def run_ours(args):
     if not args.no_per_config and world == 1:
         del d
         # the five configurations, then the longest one in the 4-bit and
-        # 2-bit caches
-        runs = [(n, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
-        runs += [("maxctx", "int4"), ("maxctx", "int2")]
-        for name, kv_dtype in runs:
-            if wl.variant_name(name, kv_dtype) == run.label:
+        # 2-bit caches, and as a one-token decode with one query head per kv
+        # head (one packed row: the CUDA-core kernel)
+        runs = [(n, None, None, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
+        runs += [("maxctx", "int4", None, None), ("maxctx", "int2", None, None), ("maxctx", None, 1, 4)]
+        for name, kv_dtype, T, Hq in runs:
+            label = wl.variant_name(name, kv_dtype, T, Hq)
+            if label == run.label:
                 continue
             torch.cuda.empty_cache()
-            r = ConfigRun(va, wl, name, dev, stream, path=args.path, kv_dtype=kv_dtype)
-            per_config[name if kv_dtype is None else f"{name}/{kv_dtype}"] = config_record(r, peak)
+            r = ConfigRun(va, wl, name, dev, stream, path=args.path, kv_dtype=kv_dtype, T=T, Hq=Hq)
+            per_config[label] = config_record(r, peak)
             r.close()
             del r
 

@@ -112,9 +112,10 @@ typedef enum {
 
 /* Which partial-attention kernel a plan uses. */
 typedef enum {
-    VA_PATH_AUTO = 0,  /* tensor cores (for every packed-row count; the CUDA-core
-                          kernel only if the tensor-core one does not fit) */
-    VA_PATH_WARP = 1,  /* CUDA-core kernel: warp-shuffle reductions, any row count */
+    VA_PATH_AUTO = 0,  /* the CUDA-core kernel for 1 or 2 packed rows per kv head,
+                          tensor cores from 3 (the measured crossover) */
+    VA_PATH_WARP = 1,  /* CUDA-core kernel: warp-shuffle reductions, any row count
+                          (4 rows per work item; more rows re-read the cache) */
     VA_PATH_MMA = 2    /* tcgen05 tensor-core kernel (TMEM accumulators) */
 } va_path;
 
@@ -241,11 +242,11 @@ const char *verify_attn_last_cuda_error_string(void);
  * VA_ERR_SCRATCH_TOO_SMALL before anything touches the device.  Nothing is
  * allocated: no cudaMalloc, no cudaFree, no allocating library call.
  *
- * It runs the partial kernel a plan picks (tensor cores) with the same one-
- * wave split, made coarser while the partials do not fit; only a problem
- * whose tensor-core partials cannot fit at any split of up to 16384 keys runs
- * the CUDA-core kernel instead (unsplit if need be), which is several times
- * slower at long contexts.  Pointer alignment is checked as for
+ * It runs the partial kernel a plan picks with a one-wave split, made
+ * coarser while the partials do not fit; only a problem whose tensor-core
+ * partials cannot fit at any split of up to 16384 keys runs the CUDA-core
+ * kernel instead (unsplit if need be), which is several times slower at long
+ * contexts with many packed rows.  Pointer alignment is checked as for
  * verify_attn_with_plan.
  *
  * The first call on a device looks up the array's device address there

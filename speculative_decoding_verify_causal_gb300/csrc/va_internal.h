@@ -99,7 +99,13 @@ size_t mma_smem_bytes(int head_dim, int kv_dtype, int num_kv_heads);
 // Geometry of each path.
 constexpr int kWarpRows = 4;     // packed rows per work item, CUDA-core kernel
 constexpr int kWarpTile = 32;    // split granularity (keys), CUDA-core kernel
-constexpr int kWarpCtasPerSm = 3;  // resident CTAs of the CUDA-core kernel per SM
+constexpr int kWarpCtasPerSm = 4;  // resident CTAs of the CUDA-core kernel per SM (3 for bf16 / 4 rows)
+// Packed rows per kv head up to which the planner picks the CUDA-core kernel:
+// measured on GB300 (D = 128 / 256, bf16 / fp8 / int8 / int4, 256 to 262k
+// tokens) it is faster than the tensor-core kernel at 1 and 2 rows (0.53-0.99
+// of its time) and slower from 3 rows on, except at the shortest contexts.
+constexpr int kWarpAutoMaxRows = 2;
+inline int auto_path(int packed_rows) { return packed_rows <= kWarpAutoMaxRows ? VA_PATH_WARP : VA_PATH_MMA; }
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)
 constexpr int kMmaTile = 64;     // keys per tile, tcgen05 kernel (N of QK^T)
 constexpr int kMmaMaxItemTokens = 16384;  // longest split of the tcgen05 kernel (page ids in smem)

@@ -15,9 +15,10 @@
 // the flag word is cleared at the start of each call and can be read back
 // with verify_attn_noalloc_flags.  The work list is staged in static host
 // buffers and copied with cudaMemcpyAsync from pageable memory.  The partial
-// kernel is the one a plan picks (tensor cores), unless its split partials
-// cannot fit in the scratch at any split length its page-id staging allows:
-// then the CUDA-core kernel runs, with splits as coarse as needed.
+// kernel is the one a plan picks (CUDA cores up to two packed rows, tensor
+// cores above), unless the tensor-core split partials cannot fit in the
+// scratch at any split length its page-id staging allows: then the CUDA-core
+// kernel runs, with splits as coarse as needed.
 #include <cmath>
 #include <mutex>
 
@@ -150,11 +151,11 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
         return VA_ERR_INVALID_ARGUMENT;
     const int bt_stride = block_table_stride > 0 ? block_table_stride : max_pages;
 
-    // Geometry: the tensor-core kernel's row groups and key tile with one
-    // wave of splits over the SMs (one resident CTA each), made coarser until
-    // the split partials fit in the scratch (at most kMmaMaxItemTokens keys
-    // per item); failing that, the CUDA-core kernel's (several CTAs per SM, no
-    // limit on the split).  A problem whose work list does not fit even
+    // Geometry: the kernel a plan picks, with one wave of splits over the
+    // SMs, made coarser until the split partials fit in the scratch; for the
+    // tensor-core kernel (one resident CTA per SM) at most kMmaMaxItemTokens
+    // keys per item, and when its partials cannot fit that way, the CUDA-core
+    // kernel's geometry (several CTAs per SM, no limit on the split).  A problem whose work list does not fit even
     // unsplit is rejected here, before any CUDA call.
     const int G = Hq / Hkv;
     const int R = G * T;
@@ -175,7 +176,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
         mma_possible = layout_for(seq_lens_host, B, Hkv, D, cap, L) && L.total <= VA_NOALLOC_SCRATCH_BYTES;
     }
     if (!warp_possible && !mma_possible) return VA_ERR_SCRATCH_TOO_SMALL;
-    const bool mma = mma_possible;
+    const bool mma = mma_possible && !(va::auto_path(R) == VA_PATH_WARP && warp_possible);
     if (!va::aligned_for(mma ? VA_PATH_MMA : VA_PATH_WARP, kv_dtype, q, k_pages, v_pages, k_scale, v_scale,
                          block_table, seq_lens, out, lse))
         return VA_ERR_INVALID_ARGUMENT;

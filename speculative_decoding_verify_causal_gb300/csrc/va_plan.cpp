@@ -105,17 +105,13 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
     return VA_OK;
 }
 
-// Tensor cores for every packed-row count: even a single row (T = 1, G = 1)
-// padded to the 128-row MMA tile runs 2-12x faster than the CUDA-core kernel
-// on GB300, from 256 to 262k cached tokens (measured for T in 1..3 and G in
-// 1..15 at D = 128 / 256), because the tile's cost is the KV stream, not the
-// padded rows.  The CUDA-core kernel remains for an explicit request and for
-// a tensor-core configuration that does not fit in shared memory.
+// The CUDA-core kernel for one or two packed rows per kv head (T = 1 or 2
+// decode with a single query head per kv head), the tensor-core kernel from
+// three rows on: the crossover measured on GB300 (va::auto_path).
 int choose_path(int R, int Hkv, const va_plan_options *opts) {
-    (void)R;
     (void)Hkv;
     int want = opts ? opts->path : VA_PATH_AUTO;
-    return want != VA_PATH_AUTO ? want : VA_PATH_MMA;
+    return want != VA_PATH_AUTO ? want : va::auto_path(R);
 }
 
 int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int dtype,

@@ -191,8 +191,14 @@ struct Geometry {
     static constexpr int KG = RPI == 1 ? 16 : 8;        // keys per batch
 };
 
+// Resident CTAs per SM the register budget is sized for: four (128 registers)
+// where that costs no spills; three for bf16 rows and the 4-row variant,
+// whose wider slices spill at 128 (measured: 4 CTAs are 7-13 % faster on the
+// 8-bit caches, 4 % slower on bf16).
+__host__ __device__ constexpr int min_ctas(int dt, int rpi) { return (dt == VA_BF16 || rpi == 4) ? 3 : kWarpCtasPerSm; }
+
 template <int D, int DT, int RPI>
-__global__ void __launch_bounds__(kThreads, kWarpCtasPerSm) warp_partial_kernel(const PartialParams p) {
+__global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kernel(const PartialParams p) {
     using Gm = Geometry<D, DT, RPI>;
     constexpr int EL = Gm::EL, KG = Gm::KG;
     constexpr bool kQuant = DT != VA_BF16;

@@ -97,16 +97,19 @@ def test_planner_fills_the_chip_for_one_long_sequence():
     assert info["max_splits"] > 1
 
 
-def test_planner_picks_tensor_cores_for_every_row_count():
-    # the tcgen05 kernel by default, down to a single packed row (measured
-    # faster than the CUDA-core kernel at every row count and context length);
-    # the CUDA-core kernel only on request
+def test_planner_picks_the_kernel_by_packed_row_count():
+    # CUDA cores for one or two packed rows per kv head, tcgen05 from three
+    # rows on (the crossover measured on GB300); either kernel on request
     big, _ = va.verify_attn_plan_describe([25016], 16, 24, 4, 256, "int8", num_sms=148)
-    small, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148)
+    two, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148)
     one, _ = va.verify_attn_plan_describe([261], 1, 1, 1, 64, "bf16", num_sms=148)
-    forced, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148, path="warp")
-    assert big["path"] == 2 and small["path"] == 2 and one["path"] == 2 and forced["path"] == 1
-    assert small["rows_per_group"] == 2 and small["num_row_groups"] == 1
+    three, _ = va.verify_attn_plan_describe([25016], 3, 4, 4, 256, "int8", num_sms=148)
+    forced, _ = va.verify_attn_plan_describe([25016], 1, 8, 4, 256, "int8", num_sms=148, path="mma")
+    assert big["path"] == 2 and three["path"] == 2 and forced["path"] == 2
+    assert two["path"] == 1 and one["path"] == 1
+    assert two["rows_per_group"] == 2 and two["num_row_groups"] == 1
+    wide, _ = va.verify_attn_plan_describe([2000], 16, 24, 4, 256, "int8", num_sms=148, path="warp")
+    assert wide["rows_per_group"] == 4 and wide["num_row_groups"] == 24  # 4 rows per CUDA-core item
     assert big["rows_per_group"] == 96 and big["num_row_groups"] == 1
     # one CTA per SM for the tensor-core kernel: about one wave of items
     assert 148 * 0.75 <= big["num_items"] <= 148

@@ -150,7 +150,7 @@ for T in (1, 5, 8, 16):
             SWEEP.append((T, G, D, dt))
 
 
-@pytest.mark.parametrize("path", ["auto", "warp"])
+@pytest.mark.parametrize("path", ["warp", "mma"])
 @pytest.mark.parametrize("T,G,D,dt", SWEEP)
 def test_shape_sweep(T, G, D, dt, path):
     Hkv = 2
