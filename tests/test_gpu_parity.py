@@ -110,6 +110,26 @@ def test_packed_cache_shapes(T, G, D, dt, path):
     compare(out, lse, ref_out, ref_lse, f"T{T} G{G} D{D} {dt} {path} {info}")
 
 
+# ------------------------------------------------------------ CUDA-core kernel: every instantiation
+WARP_ROWS = [(D, dt, T, G) for D in (64, 128, 256) for dt in ("bf16", "fp8_e4m3", "int8", "int4", "int2")
+             for (T, G) in ((1, 1), (2, 1), (1, 3), (2, 2))]
+
+
+@pytest.mark.parametrize("D,dt,T,G", WARP_ROWS)
+def test_warp_kernel_every_variant(D, dt, T, G):
+    """The CUDA-core kernel at 1, 2, 3 and 4 packed rows per kv head (its
+    one-, two- and four-row variants) for every cache type and head width:
+    a sequence shorter than one key batch, one ending mid-batch and
+    mid-page, and two split into items of a few 32-key tiles (several
+    batches per warp, the last item ragged), all against the oracle."""
+    lens = [T, 37 + T, 300 + T, 2100 + T]
+    w = wl.make_workload(8000 + D + 10 * T + G + len(dt), lens, T, G * 2, 2, D, dt, extra_pages=3)
+    out, lse, info = run_gpu(w, {"path": "warp", "tokens_per_split": 96})
+    assert info["path"] == 1 and info["rows_per_group"] == T * G
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"warp D{D} {dt} T{T} G{G} {info}")
+
+
 @pytest.mark.parametrize("dt", ["int4", "int2"])
 def test_maxctx_packed_full_output(dt):
     """262144 + 16 cached tokens (24 q / 4 kv heads, D = 256, needles at
