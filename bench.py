@@ -613,45 +613,69 @@ def run_ours(args):
     value = whole_job_rate(nbytes, args.steps, elapsed_ms, world)
 
     # end to end through the public API: pinned host inputs copied in, the
-    # result copied out, every step
+    # result copied out, every step.  Two device input sets: step i's inputs
+    # go up on a copy stream while step i - 1 computes (the host link, about
+    # 210 GB/s on this part, bounds the step; the kernel hides behind it).
     e2e = None
     if not args.no_e2e:
         host = {}
         for key in ("q", "k_pages", "v_pages", "k_scale", "v_scale", "block_table", "seq_lens"):
             t = d[key]
             host[key] = None if t is None else t.cpu().pin_memory()
-        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+        dev_sets = [{k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+                    for _ in range(2)]
         out_h = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
         lse_h = torch.empty(d["lse"].shape, dtype=d["lse"].dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
         d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
         n_e2e = max(3, min(args.steps, 20))
+        copy_stream = torch.cuda.Stream(dev)
+        uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
+        for ev in consumed:
+            ev.record(stream)
 
-        def e2e_step():
-            for k, v in host.items():
-                if v is not None:
-                    dev_in[k].copy_(v, non_blocking=True)
-            va.verify_attn_with_plan(plan, dev_in["q"], dev_in["k_pages"], dev_in["v_pages"], dev_in["k_scale"],
-                                     dev_in["v_scale"], dev_in["block_table"], dev_in["seq_lens"], w["T"],
+        def upload(i):
+            dset = dev_sets[i % 2]
+            copy_stream.wait_event(consumed[i % 2])  # the call two steps back has read this set
+            with torch.cuda.stream(copy_stream):
+                for k, v in host.items():
+                    if v is not None:
+                        dset[k].copy_(v, non_blocking=True)
+            uploaded[i % 2].record(copy_stream)
+
+        def compute(i):
+            dset = dev_sets[i % 2]
+            stream.wait_event(uploaded[i % 2])
+            va.verify_attn_with_plan(plan, dset["q"], dset["k_pages"], dset["v_pages"], dset["k_scale"],
+                                     dset["v_scale"], dset["block_table"], dset["seq_lens"], w["T"],
                                      d["out"], d["lse"], stream=stream)
-            out_h.copy_(d["out"], non_blocking=True)
-            lse_h.copy_(d["lse"], non_blocking=True)
+            consumed[i % 2].record(stream)
+            with torch.cuda.stream(stream):
+                out_h.copy_(d["out"], non_blocking=True)
+                lse_h.copy_(d["lse"], non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(2):
-                e2e_step()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n_e2e):
-                e2e_step()
-            e1.record(stream)
+        def run_steps(n):
+            upload(0)
+            for i in range(n):
+                if i + 1 < n:
+                    upload(i + 1)
+                compute(i)
+
+        run_steps(2)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        run_steps(n_e2e)
+        e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
         e2e = {"value": whole_job_rate(nbytes, 1, e2e_ms, world), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "us_per_call": e2e_ms * 1e3, "steps": n_e2e}
-        del host, dev_in
+               "d2h_bytes_per_step": d2h, "us_per_call": e2e_ms * 1e3, "steps": n_e2e,
+               "overlap": "step i+1's inputs copied on a second stream while step i computes"}
+        del host, dev_sets
 
     append = kv_append_timing(va, w, d, stream)
     lookup = lookup_draft_timing(va, wl, w)
