@@ -51,6 +51,8 @@ def parse_args():
                     "(bf16 | fp8_e4m3 | int8 | int4 | int2)")
     ap.add_argument("--T", type=int, default=None, help="replace the configuration's verify tokens")
     ap.add_argument("--Hq", type=int, default=None, help="replace the configuration's query heads")
+    ap.add_argument("--ctx", type=int, default=None,
+                    help="replace the cached context of a single-sequence configuration")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
@@ -218,7 +220,7 @@ def run_reference(args):
         return 0
     from speculative_decoding_verify_causal_gb300 import workloads as wl
     import oracle
-    w = wl.config_workload(args.config, args.kv_dtype, args.T, args.Hq)
+    w = wl.config_workload(args.config, args.kv_dtype, args.T, args.Hq, args.ctx)
     cores = oracle.max_threads(0)
     B, T, Hq = w["q"].shape[:3]
     all_rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(Hq)]
@@ -245,8 +247,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.variant_name(args.config, args.kv_dtype, args.T, args.Hq)}: "
-                               f"{wl.describe(args.config, args.kv_dtype, args.T, args.Hq)}",
+        "config": {"workload": f"{wl.variant_name(args.config, args.kv_dtype, args.T, args.Hq, args.ctx)}: "
+                               f"{wl.describe(args.config, args.kv_dtype, args.T, args.Hq, args.ctx)}",
                    "step": f"{per_step} of {len(all_rows)} query rows per step (fp64 oracle)"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{per_step} query rows per step, cycling over all rows"},
@@ -419,12 +421,12 @@ class ConfigRun:
     rotation of calls (plain, and with an event pair around every
     partial-attention kernel)."""
 
-    def __init__(self, va, wl, name, dev, stream, path="auto", kv_dtype=None, T=None, Hq=None):
+    def __init__(self, va, wl, name, dev, stream, path="auto", kv_dtype=None, T=None, Hq=None, ctx=None):
         import torch
         self.va, self.wl, self.name, self.stream = va, wl, name, stream
-        self.w = w = wl.config_workload(name, kv_dtype, T, Hq)
-        self.label = wl.variant_name(name, kv_dtype, T, Hq)
-        self.description = wl.describe(name, kv_dtype, T, Hq)
+        self.w = w = wl.config_workload(name, kv_dtype, T, Hq, ctx)
+        self.label = wl.variant_name(name, kv_dtype, T, Hq, ctx)
+        self.description = wl.describe(name, kv_dtype, T, Hq, ctx)
         self.nbytes = wl.algorithmic_bytes(w)
         self.kv_bytes = self.nbytes - 2 * w["q"].size * 2
         self.copies = 1 if self.kv_bytes > 4 * L2_BYTES else int(math.ceil(4 * L2_BYTES / self.kv_bytes))
@@ -559,7 +561,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
     peak, peak_src = peaks()
     run = ConfigRun(va, wl, args.config, dev, stream, path=args.path, kv_dtype=args.kv_dtype, T=args.T,
-                    Hq=args.Hq)
+                    Hq=args.Hq, ctx=args.ctx)
     w, d, plan, info, nbytes, copies = run.w, run.d, run.plan, run.info, run.nbytes, run.copies
     launches_per_step = 1 + (1 if info["num_split_groups"] > 0 else 0)
 
@@ -688,17 +690,19 @@ def run_ours(args):
     per_config = {run.label: head}
     if not args.no_per_config and world == 1:
         del d
-        # the five configurations, then the longest one in the 4-bit and
+        # the five configurations; the longest one at a 112k context (the
+        # other single-request length the target names), in the 4-bit and
         # 2-bit caches, and as a one-token decode with one query head per kv
         # head (one packed row: the CUDA-core kernel)
-        runs = [(n, None, None, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
-        runs += [("maxctx", "int4", None, None), ("maxctx", "int2", None, None), ("maxctx", None, 1, 4)]
-        for name, kv_dtype, T, Hq in runs:
-            label = wl.variant_name(name, kv_dtype, T, Hq)
+        runs = [(n, None, None, None, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
+        runs += [("maxctx", None, None, None, 112000), ("maxctx", "int4", None, None, None),
+                 ("maxctx", "int2", None, None, None), ("maxctx", None, 1, 4, None)]
+        for name, kv_dtype, T, Hq, ctx in runs:
+            label = wl.variant_name(name, kv_dtype, T, Hq, ctx)
             if label == run.label:
                 continue
             torch.cuda.empty_cache()
-            r = ConfigRun(va, wl, name, dev, stream, path=args.path, kv_dtype=kv_dtype, T=T, Hq=Hq)
+            r = ConfigRun(va, wl, name, dev, stream, path=args.path, kv_dtype=kv_dtype, T=T, Hq=Hq, ctx=ctx)
             per_config[label] = config_record(r, peak)
             r.close()
             del r

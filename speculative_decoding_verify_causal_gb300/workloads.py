@@ -224,17 +224,21 @@ def make_workload(seed, seq_lens, T, Hq, Hkv, D, kv_dtype, *, needles=None, peak
     }
 
 
-def variant_name(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None) -> str:
+def variant_name(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None,
+                 ctx: int | None = None) -> str:
     """Label of a named configuration with some of its fields replaced."""
-    tags = [f"{k}{v}" if k != "kv" else str(v) for k, v in (("kv", kv_dtype), ("T", T), ("Hq", Hq))
-            if v is not None]
+    tags = [f"{k}{v}" if k != "kv" else str(v)
+            for k, v in (("kv", kv_dtype), ("T", T), ("Hq", Hq), ("ctx", ctx)) if v is not None]
     return "/".join([name] + tags)
 
 
-def describe(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None) -> str:
+def describe(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None,
+             ctx: int | None = None) -> str:
     """One-line description of a (possibly modified) named configuration."""
     c = CONFIGS[name]
     d = c.description
+    if ctx is not None:
+        d = d.replace(f"{c.seq_lens[0]}+", f"{ctx}+")
     if kv_dtype is not None:
         d = d.replace(f"{c.kv_dtype.replace('_', '-')} KV", f"{kv_dtype.replace('_', '-')} KV")
     if T is not None:
@@ -244,14 +248,19 @@ def describe(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: i
     return d
 
 
-def config_workload(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None):
+def config_workload(name: str, kv_dtype: str | None = None, T: int | None = None, Hq: int | None = None,
+                    ctx: int | None = None):
     """One of the five named configurations, fully materialised.  ``kv_dtype``,
-    ``T`` (verify tokens) and ``Hq`` (query heads, a multiple of the kv
-    heads) replace its fields; the seed, context lengths and needle depths
-    stay those of the configuration."""
+    ``T`` (verify tokens), ``Hq`` (query heads, a multiple of the kv heads)
+    and ``ctx`` (the cached context of a single-sequence configuration)
+    replace its fields; the seed and the needle depths (as fractions of the
+    context) stay those of the configuration."""
     c = CONFIGS[name]
-    if T is not None or Hq is not None:
-        c = dataclasses.replace(c, T=T if T is not None else c.T, Hq=Hq if Hq is not None else c.Hq)
+    if T is not None or Hq is not None or ctx is not None:
+        if ctx is not None and c.batch > 1:
+            raise ValueError("ctx replaces the context of a single-sequence configuration")
+        c = dataclasses.replace(c, T=T if T is not None else c.T, Hq=Hq if Hq is not None else c.Hq,
+                                seq_lens=(ctx,) if ctx is not None else c.seq_lens)
     seed = 20260 + c.index
     if c.batch > 1:
         lens_rng = np.random.Generator(np.random.PCG64(seed + 1000))
@@ -267,7 +276,7 @@ def config_workload(name: str, kv_dtype: str | None = None, T: int | None = None
         def needles(rng, b, L, ctx=c.seq_lens[0]):
             return [int(math.floor(p * ctx)) for p in (0.10, 0.50, 0.90, 0.99)]
     return make_workload(seed, seq_lens, c.T, c.Hq, c.Hkv, c.D, kv_dtype or c.kv_dtype,
-                         needles=needles, peaks=c.peaks, name=variant_name(name, kv_dtype, T, Hq))
+                         needles=needles, peaks=c.peaks, name=variant_name(name, kv_dtype, T, Hq, ctx))
 
 
 def algorithmic_bytes(w) -> int:
