@@ -72,6 +72,18 @@ def test_full_size_configs_full_output(name):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+def test_112k_context_full_output():
+    """The other single-request context length the target names (112,000 +
+    16 tokens, the maxctx shapes, needles at the same depth fractions):
+    every output row against the oracle in the default plan."""
+    w = wl.config_workload("maxctx", ctx=112000)
+    out, lse, info = run_gpu(w)
+    ref_out, ref_lse = oracle.verify_attn(w)
+    stats = compare(out, lse, ref_out, ref_lse, f"maxctx/ctx112000 {info}")
+    print(f"maxctx/ctx112000: {stats}")
+    assert stats["ulp_allowance_used"] <= 1e-3 * stats["elements"], stats
+
+
 # ------------------------------------------------------------ non-unit scales
 SCALED = [(k, v, dt, T, G) for (k, v) in ((1e-3, 1e-3), (30.0, 30.0), (1.0, 1e-4), (1.0, 30.0), (30.0, 1e-4))
           for dt in ("int8", "fp8_e4m3", "int4", "int2") for (T, G) in ((16, 6), (1, 4))]
