@@ -690,10 +690,10 @@ def run_ours(args):
     per_config = {run.label: head}
     if not args.no_per_config and world == 1:
         del d
-        # the five configurations; the longest one at a 112k context (the
-        # other single-request length the target names), in the 4-bit and
-        # 2-bit caches, and as a one-token decode with one query head per kv
-        # head (one packed row: the CUDA-core kernel)
+        # the five configurations; the longest one at a 112k context (where
+        # "I pushed Qwen3.8-27B to 381 tps ..." measures single-user decode),
+        # in the 4-bit and 2-bit caches, and as a one-token decode with one
+        # query head per kv head (one packed row: the CUDA-core kernel)
         runs = [(n, None, None, None, None) for n in ("tiny", "mtp4", "batched", "maxctx", "lookup16")]
         runs += [("maxctx", None, None, None, 112000), ("maxctx", "int4", None, None, None),
                  ("maxctx", "int2", None, None, None), ("maxctx", None, 1, 4, None)]

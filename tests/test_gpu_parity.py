@@ -73,9 +73,10 @@ def test_full_size_configs_full_output(name):
 
 
 def test_112k_context_full_output():
-    """The other single-request context length the target names (112,000 +
-    16 tokens, the maxctx shapes, needles at the same depth fractions):
-    every output row against the oracle in the default plan."""
+    """A 112k context ("I pushed Qwen3.8-27B to 381 tps for a single request
+    on a RTX 3090" measures single-user decode there): 112,000 + 16 tokens,
+    the maxctx shapes, needles at the same depth fractions; every output row
+    against the oracle in the default plan."""
     w = wl.config_workload("maxctx", ctx=112000)
     out, lse, info = run_gpu(w)
     ref_out, ref_lse = oracle.verify_attn(w)
