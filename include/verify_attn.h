@@ -193,6 +193,21 @@ int verify_attn_plan_describe(const int32_t *seq_lens_host, int num_seqs, int T,
                               const va_plan_options *opts, va_plan_info *info,
                               int32_t *items, int max_items);
 
+/* Host-side check of a batch's paging inputs before they go to the device
+ * (no CUDA call, usable without a GPU): every sequence length satisfies
+ * T <= seq_lens[b] <= 16 * block_table_stride, and every block-table entry
+ * that a sequence uses (entries 0 .. ceil(L_b / 16) - 1 of row b) lies in
+ * [0, num_pages).  Layouts as for verify_attn, both arrays in host memory.
+ * Returns VA_OK, or VA_ERR_INVALID_ARGUMENT for null pointers, non-positive
+ * sizes or the first violation found; *bad_seq and *bad_block (either may be
+ * NULL) then name it: the sequence, and the block index within its row (-1
+ * when the length itself is at fault); both are -1 on success.  The device
+ * kernels make the same page check themselves when a plan knows num_pages;
+ * this call lets a caller reject a bad batch before launching anything. */
+int verify_attn_validate_host(const int32_t *seq_lens_host, int num_seqs, int T,
+                              const int32_t *block_table_host, int block_table_stride,
+                              int num_pages, int *bad_seq, int *bad_block);
+
 /* Read (and if clear != 0, reset) the plan's device flag word:
  *   bit 0 (1) = a block-table entry outside [0, num_pages) was skipped;
  *   bit 1 (2) = a device seq_lens value differed from the planned one;

@@ -108,6 +108,8 @@ def _load():
         lib.verify_attn_accept_workspace_bytes.restype = ctypes.c_size_t
         lib.verify_attn_accept.argtypes = [P, P, P, P, I, I, I, ctypes.c_uint64, P, P, P, P]
         lib.verify_attn_accept.restype = I
+        lib.verify_attn_validate_host.argtypes = [P, I, I, P, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+        lib.verify_attn_validate_host.restype = I
         for f in ("verify_attn_plan", "verify_attn_plan_ex", "verify_attn", "verify_attn_with_plan",
                   "verify_attn_plan_get_info", "verify_attn_plan_describe", "verify_attn_plan_device_flags"):
             getattr(lib, f).restype = I
@@ -195,6 +197,30 @@ def verify_attn_plan(seq_lens, T, num_q_heads, num_kv_heads, head_dim, kv_dtype,
 
 def verify_attn_plan_destroy(plan: Plan):
     plan.destroy()
+
+
+def verify_attn_validate_host(seq_lens, T, block_table, num_pages):
+    """Host check of the paging inputs (no GPU needed).  Returns None when
+    they are valid, else (sequence, block index or -1) of the first fault."""
+    lens = _host_lens(seq_lens)
+    try:
+        import torch
+        if isinstance(block_table, torch.Tensor):
+            block_table = block_table.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if bt.ndim != 2 or bt.shape[0] != len(lens):
+        raise ValueError("block_table must be [num_seqs, stride]")
+    bad_seq, bad_block = ctypes.c_int(-1), ctypes.c_int(-1)
+    rc = _load().verify_attn_validate_host(lens.ctypes.data_as(ctypes.c_void_p), len(lens), int(T),
+                                           bt.ctypes.data_as(ctypes.c_void_p), bt.shape[1], int(num_pages),
+                                           ctypes.byref(bad_seq), ctypes.byref(bad_block))
+    if rc == 0:
+        return None
+    if bad_seq.value < 0:
+        _check(rc, "verify_attn_validate_host")
+    return bad_seq.value, bad_block.value
 
 
 def verify_attn_plan_get_info(plan: Plan) -> dict:
@@ -455,5 +481,6 @@ __all__ = [
     "verify_attn_plan_set_events",
     "verify_attn_plan", "verify_attn", "verify_attn_with_plan", "verify_attn_plan_destroy",
     "verify_attn_status_string", "verify_attn_plan_get_info", "verify_attn_plan_describe",
-    "verify_attn_plan_device_flags", "Plan", "VerifyAttnError", "library", "LIB_PATH",
+    "verify_attn_plan_device_flags", "verify_attn_validate_host", "Plan", "VerifyAttnError", "library",
+    "LIB_PATH",
 ]

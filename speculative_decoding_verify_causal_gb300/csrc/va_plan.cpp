@@ -301,6 +301,31 @@ const char *verify_attn_last_cuda_error_string(void) {
     return cudaGetErrorString(static_cast<cudaError_t>(t_last_cuda_error));
 }
 
+int verify_attn_validate_host(const int32_t *seq_lens, int B, int T, const int32_t *block_table,
+                              int bt_stride, int num_pages, int *bad_seq, int *bad_block) {
+    if (bad_seq) *bad_seq = -1;
+    if (bad_block) *bad_block = -1;
+    if (!seq_lens || !block_table || B < 1 || T < 1 || bt_stride < 1 || num_pages < 1)
+        return VA_ERR_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b) {
+        const long long L = seq_lens[b];
+        if (L < T || L > (long long)VA_PAGE_SIZE * bt_stride) {
+            if (bad_seq) *bad_seq = b;
+            return VA_ERR_INVALID_ARGUMENT;
+        }
+        const int used = (int)((L + VA_PAGE_SIZE - 1) / VA_PAGE_SIZE);
+        const int32_t *row = block_table + (size_t)b * bt_stride;
+        for (int i = 0; i < used; ++i) {
+            if (row[i] < 0 || row[i] >= num_pages) {
+                if (bad_seq) *bad_seq = b;
+                if (bad_block) *bad_block = i;
+                return VA_ERR_INVALID_ARGUMENT;
+            }
+        }
+    }
+    return VA_OK;
+}
+
 const char *verify_attn_status_string(int status) {
     switch (status) {
     case VA_OK: return "ok";

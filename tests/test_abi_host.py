@@ -172,3 +172,25 @@ def test_accept_workspace_size(B, T):
     assert lib.verify_attn_accept_workspace_bytes(B, T) == 32 * B * (T + 1) + 16 * B
     assert lib.verify_attn_accept_workspace_bytes(0, T) == 0
     assert lib.verify_attn_accept_workspace_bytes(B, 0) == 0
+
+
+def test_validate_host_paging_inputs():
+    # host-only check of seq_lens and the block-table entries in use
+    rng = np.random.default_rng(5)
+    lens = np.array([40, 16, 5, 33], np.int32)
+    bt = rng.integers(0, 50, size=(4, 3)).astype(np.int32)
+    assert va.verify_attn_validate_host(lens, 5, bt, 50) is None
+    bt_unused = bt.copy()
+    bt_unused[1, 1:] = -7           # sequence 1 uses one page: later entries are not read
+    bt_unused[2, 1:] = 999
+    assert va.verify_attn_validate_host(lens, 5, bt_unused, 50) is None
+    bad = bt.copy()
+    bad[3, 2] = 50                  # == num_pages: outside the pool
+    assert va.verify_attn_validate_host(lens, 5, bad, 50) == (3, 2)
+    bad = bt.copy()
+    bad[0, 1] = -1
+    assert va.verify_attn_validate_host(lens, 5, bad, 50) == (0, 1)
+    assert va.verify_attn_validate_host(np.array([40, 16, 4, 33], np.int32), 5, bt, 50) == (2, -1)  # L < T
+    assert va.verify_attn_validate_host(np.array([40, 16, 5, 49], np.int32), 5, bt, 50) == (3, -1)  # > 16 * stride
+    with pytest.raises(va.VerifyAttnError):
+        va.verify_attn_validate_host(lens, 5, bt, 0)
