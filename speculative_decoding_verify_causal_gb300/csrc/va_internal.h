@@ -99,11 +99,23 @@ size_t mma_smem_bytes(int head_dim, int kv_dtype, int num_kv_heads);
 // Geometry of each path.
 constexpr int kWarpRows = 4;     // packed rows per work item, CUDA-core kernel
 constexpr int kWarpTile = 32;    // split granularity (keys), CUDA-core kernel
-constexpr int kWarpCtasPerSm = 4;  // resident CTAs of the CUDA-core kernel per SM (3 for bf16 / 4 rows)
+constexpr int kWarpCtasPerSm = 4;  // resident CTAs of the CUDA-core kernel per SM (most variants)
+// The CUDA-core kernel's register budget, and with it its resident CTAs per
+// SM: four (128 registers) where that costs no spills, three for bf16 rows
+// and the 4-row variant, whose wider slices spill at 128 (measured: 4 CTAs are
+// 7-13 % faster on the 8-bit caches, 4 % slower on bf16).  The planner sizes
+// the split for the same count, so that a plan is one wave.
+__host__ __device__ constexpr int warp_rows_variant(int rows_per_item) {
+    return rows_per_item <= 1 ? 1 : rows_per_item <= 2 ? 2 : 4;
+}
+__host__ __device__ constexpr int warp_ctas_per_sm(int kv_dtype, int rows_per_item) {
+    return (kv_dtype == VA_BF16 || warp_rows_variant(rows_per_item) == 4) ? 3 : kWarpCtasPerSm;
+}
 // Packed rows per kv head up to which the planner picks the CUDA-core kernel:
 // measured on GB300 (D = 128 / 256, bf16 / fp8 / int8 / int4, 256 to 262k
-// tokens) it is faster than the tensor-core kernel at 1 and 2 rows (0.53-0.99
-// of its time) and slower from 3 rows on, except at the shortest contexts.
+// tokens) it takes 0.54-0.81 of the tensor-core kernel's time at 1 row and
+// 0.62-0.92 at 2, and from 3 rows on it is faster only at a few hundred
+// tokens (0.94-1.21 of the time from 4k tokens).
 constexpr int kWarpAutoMaxRows = 2;
 inline int auto_path(int packed_rows) { return packed_rows <= kWarpAutoMaxRows ? VA_PATH_WARP : VA_PATH_MMA; }
 constexpr int kMmaRows = 128;    // packed rows per work item, tcgen05 kernel (M)

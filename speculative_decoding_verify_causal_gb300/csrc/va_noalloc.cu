@@ -187,7 +187,7 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     if (rc != VA_OK) return rc;
     geometry(mma, L);
     const int cap = mma ? (max_len < va::kMmaMaxItemTokens ? max_len : va::kMmaMaxItemTokens) : max_len;
-    const long long slots = (long long)(mma ? 1 : va::kWarpCtasPerSm) * num_sms;
+    const long long slots = (long long)(mma ? 1 : va::warp_ctas_per_sm(kv_dtype, L.rows_per_group)) * num_sms;
     long long c = (total_len * Hkv * L.num_row_groups + slots - 1) / slots;
     c = (c + L.tile - 1) / L.tile * L.tile;
     if (c < 4 * L.tile) c = 4 * L.tile;

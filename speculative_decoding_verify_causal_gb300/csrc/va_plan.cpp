@@ -127,9 +127,11 @@ int plan_geometry(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D,
     const bool mma = g.path == VA_PATH_MMA;
     const int max_rows = mma ? va::kMmaRows : va::kWarpRows;
     g.tile = mma ? va::kMmaTile : va::kWarpTile;
-    g.slots = mma ? num_sms : num_sms * va::kWarpCtasPerSm;  // the tcgen05 kernel holds a whole SM
     g.num_row_groups = (R + max_rows - 1) / max_rows;
     g.rows_per_group = (R + g.num_row_groups - 1) / g.num_row_groups;
+    // the tcgen05 kernel holds a whole SM; the CUDA-core kernel's residency
+    // depends on its variant
+    g.slots = mma ? num_sms : num_sms * va::warp_ctas_per_sm(dtype, g.rows_per_group);
 
     int maxL = 0;
     double total = 0.0;

@@ -81,11 +81,84 @@ struct Slice {
     }
 };
 
-// The slice's EL codes as exact fp32 values (the code, not yet scaled).
-// Integers: a code c with offset u = c + 2^(b-1) in [0, 2^b) is placed in the
-// low mantissa bits of 2^23 (u XOR-ed into 0x4B000000 | 2^(b-1) flips the
-// sign bit of the two's-complement field into that offset), and 2^23 plus
-// the offset is subtracted: both steps are exact.
+// Packed fp32 pairs (sm_100+): each half of fma/add/mul.f32x2 is one
+// IEEE-rounded fp32 operation, the same result as the scalar instruction, at
+// half the issue cost.
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pk2f(float lo, float hi) { return pk2(__float_as_uint(lo), __float_as_uint(hi)); }
+__device__ __forceinline__ float2 upk2(uint64_t r) {
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(r));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The slice's EL codes as EL / 2 exact fp32 pairs (elements 2i, 2i + 1), the
+// codes themselves, not yet scaled.  Integers: a code c with offset
+// u = c + 2^(b-1) in [0, 2^b) is placed in the low mantissa bits of 2^23 (u
+// XOR-ed into 0x4B000000 | 2^(b-1) flips the sign bit of the two's-complement
+// field into that offset), and 2^23 plus the offset is subtracted with one
+// paired add: both steps are exact.  bf16 is a shift; fp8-e4m3 goes through
+// the hardware's exact conversion to fp16.
+template <int DT, int EL>
+__device__ __forceinline__ void decode2(const uint32_t *w, uint64_t *f) {
+    if constexpr (DT == VA_BF16) {
+#pragma unroll
+        for (int i = 0; i < EL / 2; ++i) f[i] = pk2(w[i] << 16, w[i] & 0xFFFF0000u);
+    } else if constexpr (DT == VA_INT8) {
+        const uint64_t off = pk2f(-8388736.0f, -8388736.0f);
+#pragma unroll
+        for (int i = 0; i < EL / 2; ++i) {
+            const uint32_t x = w[i / 2] ^ 0x80808080u;
+            const int k = 2 * (i % 2);
+            f[i] = add2(pk2(__byte_perm(x, 0x4B000000u, 0x7440 + k), __byte_perm(x, 0x4B000000u, 0x7441 + k)), off);
+        }
+    } else if constexpr (DT == VA_INT4) {
+        const uint64_t off = pk2f(-8388616.0f, -8388616.0f);
+#pragma unroll
+        for (int i = 0; i < EL / 2; ++i) {
+            const uint32_t x = w[i / 4] >> (8 * (i % 4));
+            f[i] = add2(pk2((x & 0xFu) ^ 0x4B000008u, ((x >> 4) & 0xFu) ^ 0x4B000008u), off);
+        }
+    } else if constexpr (DT == VA_INT2) {
+        const uint64_t off = pk2f(-8388610.0f, -8388610.0f);
+#pragma unroll
+        for (int i = 0; i < EL / 2; ++i) {
+            const uint32_t x = w[i / 8] >> (4 * (i % 8));
+            f[i] = add2(pk2((x & 0x3u) ^ 0x4B000002u, ((x >> 2) & 0x3u) ^ 0x4B000002u), off);
+        }
+    } else {  // fp8-e4m3
+#pragma unroll
+        for (int i = 0; i < EL / 2; ++i) {
+            const uint32_t x = w[i / 2] >> (16 * (i % 2));
+            __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xFFFFu), __NV_E4M3);
+            const float2 v = __half22float2(*reinterpret_cast<__half2 *>(&h));
+            f[i] = pk2f(v.x, v.y);
+        }
+    }
+}
+
+// The same codes as plain fp32 values, one subtract per element: the form the
+// one-row kernel uses (it is bound by memory, and the pair form's extra
+// combining add per key costs it more than the paired arithmetic saves).
 template <int DT, int EL>
 __device__ __forceinline__ void decode(const uint32_t *w, float *f) {
     if constexpr (DT == VA_BF16) {
@@ -191,14 +264,8 @@ struct Geometry {
     static constexpr int KG = RPI == 1 ? 16 : 8;        // keys per batch
 };
 
-// Resident CTAs per SM the register budget is sized for: four (128 registers)
-// where that costs no spills; three for bf16 rows and the 4-row variant,
-// whose wider slices spill at 128 (measured: 4 CTAs are 7-13 % faster on the
-// 8-bit caches, 4 % slower on bf16).
-__host__ __device__ constexpr int min_ctas(int dt, int rpi) { return (dt == VA_BF16 || rpi == 4) ? 3 : kWarpCtasPerSm; }
-
 template <int D, int DT, int RPI>
-__global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kernel(const PartialParams p) {
+__global__ void __launch_bounds__(kThreads, warp_ctas_per_sm(DT, RPI)) warp_partial_kernel(const PartialParams p) {
     using Gm = Geometry<D, DT, RPI>;
     constexpr int EL = Gm::EL, KG = Gm::KG;
     constexpr bool kQuant = DT != VA_BF16;
@@ -233,13 +300,18 @@ __global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kern
         }
     }
 
-    float m_run[RPI], l_run[RPI], acc[RPI][EL];
+    uint64_t q2[RPI][EL / 2];  // q as fp32 pairs
+    float m_run[RPI], l_run[RPI];
+    uint64_t acc[RPI][EL / 2];  // this lane's slice of O as fp32 pairs
 #pragma unroll
     for (int r = 0; r < RPI; ++r) {
         m_run[r] = -INFINITY;
         l_run[r] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EL; ++e) acc[r][e] = 0.f;
+        for (int i = 0; i < EL / 2; ++i) {
+            q2[r][i] = pk2f(q[r][2 * i], q[r][2 * i + 1]);
+            acc[r][i] = 0ull;  // (+0.0f, +0.0f)
+        }
     }
 
     const uint8_t *kbase = static_cast<const uint8_t *>(p.k_pages);
@@ -290,14 +362,24 @@ __global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kern
             float part[RPI][KG];
 #pragma unroll
             for (int k = 0; k < KG; ++k) {
-                float f[EL];
-                decode<DT, EL>(k_raw[k].w, f);
-#pragma unroll
-                for (int r = 0; r < RPI; ++r) {
+                if constexpr (RPI == 1) {
+                    float f[EL];
+                    decode<DT, EL>(k_raw[k].w, f);
                     float a = 0.f;
 #pragma unroll
-                    for (int e = 0; e < EL; ++e) a = fmaf(q[r][e], f[e], a);
-                    part[r][k] = a;
+                    for (int e = 0; e < EL; ++e) a = fmaf(q[0][e], f[e], a);
+                    part[0][k] = a;
+                } else {
+                    uint64_t f[EL / 2];
+                    decode2<DT, EL>(k_raw[k].w, f);
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r) {
+                        uint64_t a = 0ull;
+#pragma unroll
+                        for (int i = 0; i < EL / 2; ++i) a = fma2(q2[r][i], f[i], a);
+                        const float2 h = upk2(a);
+                        part[r][k] = h.x + h.y;
+                    }
                 }
             }
 #pragma unroll
@@ -317,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kern
                 const float alpha = m_run[r] == -INFINITY ? 0.f : ex2_approx(m_run[r] - bmax);
                 m_run[r] = bmax;
                 l_run[r] *= alpha;
+                const uint64_t a2 = pk2f(alpha, alpha);
 #pragma unroll
-                for (int e = 0; e < EL; ++e) acc[r][e] *= alpha;
+                for (int i = 0; i < EL / 2; ++i) acc[r][i] = mul2(acc[r][i], a2);
             }
             const float pr = s[r] == -INFINITY ? 0.f : ex2_approx(s[r] - m_run[r]);
             if (key_owner) l_run[r] += pr;
@@ -326,13 +409,25 @@ __global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kern
         }
 #pragma unroll
         for (int k = 0; k < KG; ++k) {
-            float f[EL];
-            decode<DT, EL>(v_raw[k].w, f);
+            if constexpr (RPI == 1) {
+                float f[EL];
+                decode<DT, EL>(v_raw[k].w, f);
+                const float w = __shfl_sync(0xffffffffu, pv[0], lane_of_key<KG>(k));
 #pragma unroll
-            for (int r = 0; r < RPI; ++r) {
-                const float w = __shfl_sync(0xffffffffu, pv[r], lane_of_key<KG>(k));
+                for (int i = 0; i < EL / 2; ++i) {
+                    const float2 o = upk2(acc[0][i]);
+                    acc[0][i] = pk2f(fmaf(w, f[2 * i], o.x), fmaf(w, f[2 * i + 1], o.y));
+                }
+            } else {
+                uint64_t f[EL / 2];
+                decode2<DT, EL>(v_raw[k].w, f);
 #pragma unroll
-                for (int e = 0; e < EL; ++e) acc[r][e] = fmaf(w, f[e], acc[r][e]);
+                for (int r = 0; r < RPI; ++r) {
+                    const float w = __shfl_sync(0xffffffffu, pv[r], lane_of_key<KG>(k));
+                    const uint64_t w2 = pk2f(w, w);
+#pragma unroll
+                    for (int i = 0; i < EL / 2; ++i) acc[r][i] = fma2(w2, f[i], acc[r][i]);
+                }
             }
         }
     }
@@ -348,7 +443,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas(DT, RPI)) warp_partial_kern
             sm_l[warp][r] = l;
         }
 #pragma unroll
-        for (int e = 0; e < EL; ++e) sm_o[warp][r][lane * EL + e] = acc[r][e];
+        for (int i = 0; i < EL / 2; ++i) {
+            const float2 o = upk2(acc[r][i]);
+            sm_o[warp][r][lane * EL + 2 * i] = o.x;
+            sm_o[warp][r][lane * EL + 2 * i + 1] = o.y;
+        }
     }
     __syncthreads();
 #pragma unroll
@@ -396,9 +495,11 @@ cudaError_t launch_one(const PartialParams &p, int n, cudaStream_t s) {
 
 template <int D, int DT>
 cudaError_t launch_rows(const PartialParams &p, int n, cudaStream_t s) {
-    if (p.rows_per_group <= 1) return launch_one<D, DT, 1>(p, n, s);
-    if (p.rows_per_group <= 2) return launch_one<D, DT, 2>(p, n, s);
-    return launch_one<D, DT, 4>(p, n, s);
+    switch (warp_rows_variant(p.rows_per_group)) {
+    case 1: return launch_one<D, DT, 1>(p, n, s);
+    case 2: return launch_one<D, DT, 2>(p, n, s);
+    default: return launch_one<D, DT, 4>(p, n, s);
+    }
 }
 
 template <int D>
