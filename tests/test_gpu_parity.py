@@ -123,6 +123,34 @@ def test_packed_cache_shapes(T, G, D, dt, path):
     compare(out, lse, ref_out, ref_lse, f"T{T} G{G} D{D} {dt} {path} {info}")
 
 
+# ------------------------------------------------------------ wide shapes
+@pytest.mark.parametrize("path", ["auto", "warp"])
+@pytest.mark.parametrize("T,G,D,dt", [(24, 8, 128, "int8"), (16, 15, 256, "fp8_e4m3"), (32, 5, 64, "bf16")])
+def test_more_rows_than_one_mma_tile(T, G, D, dt, path):
+    """Packed rows per kv head above the tensor-core tile's 128 (192, 240,
+    160): several row groups per kv head, each re-reading the cache, with a
+    split so that the combine merges every group."""
+    w = wl.make_workload(9100 + T * G + D, [T + 3, 700 + T, 2000 + T], T, G * 2, 2, D, dt)
+    out, lse, info = run_gpu(w, {"path": path, "tokens_per_split": 256})
+    assert info["num_row_groups"] > 1
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"T{T} G{G} D{D} {dt} {path} {info}")
+
+
+@pytest.mark.parametrize("T,G", [(1, 1), (1, 4), (5, 6)])
+def test_wide_batch_many_heads(T, G):
+    """256 sequences of 1 to 2,000 cached tokens (several shorter than one
+    page) with 8 kv heads, D = 128, int8, in the default plan: the packed-row
+    crossover picks the CUDA-core kernel at one row and tensor cores above."""
+    rng = np.random.default_rng(77 + T + G)
+    lens = [int(x) + T for x in rng.integers(1, 2000, 256)]
+    w = wl.make_workload(9300 + T + G, lens, T, G * 8, 8, 128, "int8")
+    out, lse, info = run_gpu(w)
+    assert info["path"] == (1 if T * G <= 2 else 2)
+    ref_out, ref_lse = oracle.verify_attn(w)
+    compare(out, lse, ref_out, ref_lse, f"B256 T{T} G{G} {info}")
+
+
 # ------------------------------------------------------------ CUDA-core kernel: every instantiation
 WARP_ROWS = [(D, dt, T, G) for D in (64, 128, 256) for dt in ("bf16", "fp8_e4m3", "int8", "int4", "int2")
              for (T, G) in ((1, 1), (2, 1), (1, 3), (2, 2))]
