@@ -181,7 +181,7 @@ def test_softmax_rows_sum_to_one(dt):
     np.testing.assert_allclose(out, 1.0, rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "int8", "int4", "int2"])
 def test_T1_is_plain_decode_of_last_verify_token(dt):
     T = 5
     w = small_workload(11, [70], T, 4, 2, 16, dt)
@@ -204,14 +204,17 @@ def test_T1_is_plain_decode_of_last_verify_token(dt):
                                    rtol=0, atol=1e-12)
 
 
-def test_identical_keys_closed_form():
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8", "int4", "int2"])
+def test_identical_keys_closed_form(dt):
     T, Hq, Hkv, D, L = 6, 4, 2, 16, 40
-    w = small_workload(13, [L], T, Hq, Hkv, D, "bf16")
+    w = small_workload(13, [L], T, Hq, Hkv, D, dt)
     kp = w["k_pages"]
-    # every key row of each kv head equal to the head's first row
+    # every key row (and its scale) of each kv head equal to the head's first row
     for g in range(Hkv):
         row0 = kp[w["block_table"][0, 0], 0, g].copy()
         kp[:, :, g, :] = row0
+        if w["k_scale"] is not None:
+            w["k_scale"][:, :, g] = w["k_scale"][w["block_table"][0, 0], 0, g]
     out, lse = oracle.verify_attn(w)
     q = q_f64(w)[0]  # [T, Hq, D]
     K = dense_kv(w, "k")[0]
@@ -243,7 +246,7 @@ def test_split_lse_merge_equals_direct(split):
     assert l_m == -math.inf and not o_m.any()
 
 
-@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "fp8_e4m3", "int8", "int4", "int2"])
 def test_page_permutation_invariance(dt):
     w = small_workload(19, [45, 33], 3, 4, 2, 16, dt, extra_pages=4)
     out, lse = oracle.verify_attn(w)
