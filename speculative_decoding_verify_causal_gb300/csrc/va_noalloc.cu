@@ -155,8 +155,9 @@ extern "C" int verify_attn_noalloc(const int32_t *seq_lens_host, int B, int T, i
     // SMs, made coarser until the split partials fit in the scratch; for the
     // tensor-core kernel (one resident CTA per SM) at most kMmaMaxItemTokens
     // keys per item, and when its partials cannot fit that way, the CUDA-core
-    // kernel's geometry (several CTAs per SM, no limit on the split).  A problem whose work list does not fit even
-    // unsplit is rejected here, before any CUDA call.
+    // kernel's geometry (several CTAs per SM, no limit on the split).  A
+    // problem whose work list does not fit even unsplit is rejected here,
+    // before any CUDA call.
     const int G = Hq / Hkv;
     const int R = G * T;
     auto geometry = [&](bool mma, Layout &L) {

@@ -105,8 +105,8 @@ int validate(const int32_t *seq_lens, int B, int T, int Hq, int Hkv, int D, int 
     return VA_OK;
 }
 
-// The CUDA-core kernel for one or two packed rows per kv head (T = 1 or 2
-// decode with a single query head per kv head), the tensor-core kernel from
+// The CUDA-core kernel for one or two packed rows per kv head (a T = 1 decode
+// with one or two query heads per kv head, say), the tensor-core kernel from
 // three rows on: the crossover measured on GB300 (va::auto_path).
 int choose_path(int R, int Hkv, const va_plan_options *opts) {
     (void)Hkv;
