@@ -99,7 +99,7 @@ typedef enum {
 
 typedef enum {
     VA_OK = 0,
-    VA_ERR_INVALID_ARGUMENT = -1, /* null pointer, T < 1, Hq % Hkv != 0, L_b < T ... */
+    VA_ERR_INVALID_ARGUMENT = -1, /* null or misaligned pointer, T < 1, Hq % Hkv != 0, L_b < T ... */
     VA_ERR_UNSUPPORTED = -2,      /* head_dim not in {64, 128, 256}, unknown dtype */
     VA_ERR_PLAN_MISMATCH = -3,    /* call arguments disagree with the plan */
     VA_ERR_NO_PLAN = -4,          /* verify_attn with no current plan on this thread */
