@@ -194,3 +194,33 @@ def test_validate_host_paging_inputs():
     assert va.verify_attn_validate_host(np.array([40, 16, 5, 49], np.int32), 5, bt, 50) == (3, -1)  # > 16 * stride
     with pytest.raises(va.VerifyAttnError):
         va.verify_attn_validate_host(lens, 5, bt, 0)
+
+
+def test_planner_random_shapes_cover_every_key_and_respect_kernel_limits():
+    # randomised shapes through the host planner: every (sequence, kv head,
+    # row group) key range covered exactly once, item starts on the kernel's
+    # split tile, tensor-core items no longer than the page ids it stages,
+    # CUDA-core items no wider than its 4-row variant, and the path the
+    # packed-row crossover names
+    rng = np.random.default_rng(2026)
+    for _ in range(150):
+        B = int(rng.integers(1, 40))
+        T = int(rng.integers(1, 17))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.integers(1, 9))
+        D = int(rng.choice([64, 128, 256]))
+        dt = str(rng.choice(["bf16", "fp8_e4m3", "int8", "int4", "int2"]))
+        lens = [int(x) + T for x in rng.integers(0, int(rng.choice([50, 2000, 70000])), B)]
+        path = str(rng.choice(["auto", "warp", "mma"]))
+        sms = int(rng.choice([16, 148, 152]))
+        info, items = va.verify_attn_plan_describe(lens, T, G * Hkv, Hkv, D, dt, num_sms=sms, path=path)
+        assert info["num_items"] == len(items) > 0
+        _check_cover(lens, T, G * Hkv, Hkv, items, info)
+        want = {"warp": 1, "mma": 2}.get(path, 1 if G * T <= 2 else 2)
+        assert info["path"] == want
+        tile = 64 if want == 2 else 32
+        assert all(k0 % tile == 0 for _, _, _, k0, _ in items)
+        if want == 2:
+            assert max(k1 - k0 for _, _, _, k0, k1 in items) <= 16384
+        else:
+            assert info["rows_per_group"] <= 4
