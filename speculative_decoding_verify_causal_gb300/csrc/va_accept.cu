@@ -5,7 +5,7 @@
 // rejection emits a sample of max(0, p - q), a full acceptance the bonus
 // sample of p_T, both as exponential races with Philox4x32-10 Gumbel variates.
 //
-// Two kernels.  stats_kernel, one thread-block cluster of kCluster CTAs per
+// Two kernels.  stats_kernel, one thread-block cluster of 2, 4 or 8 CTAs per
 // (sequence, position), each CTA a slice of the vocabulary, partial results
 // exchanged through distributed shared memory (combined in rank order, so
 // every CTA and every run gets the same binary32 value): the maximum and
@@ -20,6 +20,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "va_internal.h"
 #include "va_sm100.cuh"
@@ -30,7 +31,17 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 1024;
-constexpr int kCluster = 8;          // CTAs per vocabulary row in the statistics (portable cluster size)
+// CTAs per vocabulary row in the statistics: 8 for up to 8 rows, 4 while the
+// rows fit one wave of the GPU at that width, else 2 (measured on GB300 at
+// 151,936 entries, greedy / sampled: 6 rows 6.8 / 14.2 us with 8 against
+// 7.3 / 15.4 with 4; 17 rows 7.4 / 15.7 with 4 against 9.0 / 18.3 with 8;
+// 384 rows 49.6 / 129.8 with 2 against 81.6 / 192.3 with 8 and 48.7 / 144.6
+// with 1).  Larger slices per CTA amortise the cluster's barriers until too
+// few SMs are left working.
+constexpr int kClusterMax = 8;
+constexpr int kClusterWide = 4;
+constexpr int kClusterNarrow = 2;
+constexpr int kClusterMaxRows = 8;
 constexpr int kRaceThreads = 256;    // decide_kernel CTA size
 constexpr int kRacePerThread = 4;    // vocabulary entries per race thread (sets the row of CTAs)
 constexpr int kMaxRaceCtas = 1024;
@@ -210,11 +221,25 @@ __device__ void row_stats(const float *row, int V, float scale, bool want_lse, u
     const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     int lo, hi;
     slice(V, lo, hi, vec ? 4 : 1);
-    unsigned long long k = 0;
+    // per thread: the largest value and its first index (a thread visits its
+    // indices in increasing order, so a strict compare keeps the smallest
+    // index of a tie); the 64-bit (value, index) key is formed once per thread
+    float tmax = -INFINITY;
+    int tidx = -1;
     row_pass(row, lo, hi, vec, [&](int i, float x) {
-        const unsigned long long c = vkey(x * scale, i);
-        k = c > k ? c : k;
+        const float v = x * scale;
+        if (v > tmax) {
+            tmax = v;
+            tidx = i;
+        }
     });
+    unsigned long long k = 0;
+    if (tidx >= 0) {
+        k = vkey(tmax, tidx);
+    } else {  // nothing above -inf here: the smallest index this thread visited
+        const int first = vec ? 4 * ((lo >> 2) + (int)threadIdx.x) : lo + (int)threadIdx.x;
+        if (first < hi) k = vkey(-INFINITY, first);
+    }
     k = cluster_max_u64(block_max_u64(k, redk), slot_k);
     argmax = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
     if (!want_lse) return;
@@ -322,16 +347,16 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
     write_tokens(p, b, n, (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull)));
 }
 
-// Launch with a (kCluster, 1, 1) cluster and programmatic dependent launch.
+// Launch with a (cluster, 1, 1) cluster and programmatic dependent launch.
 template <typename K>
-cudaError_t launch_cluster(K kernel, dim3 grid, cudaStream_t s, const AcceptParams &p) {
+cudaError_t launch_cluster(K kernel, dim3 grid, int cluster, cudaStream_t s, const AcceptParams &p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -371,12 +396,40 @@ extern "C" int verify_attn_accept(const float *target_logits, const float *draft
     p.T = T;
     p.V = vocab;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = va::launch_cluster(va::stats_kernel, dim3(va::kCluster, T + 1, num_seqs), s, p);
-    // a row of race CTAs per sequence, kRacePerThread vocabulary entries per thread
-    const int nrace = (int)std::min<long long>(
-        va::kMaxRaceCtas, std::max<long long>(1, ((long long)vocab + va::kRaceThreads * va::kRacePerThread - 1) /
-                                                     (va::kRaceThreads * va::kRacePerThread)));
-    if (e == cudaSuccess) e = va::launch_pdl(va::decide_kernel, dim3(nrace, num_seqs), dim3(va::kRaceThreads), 0, s, p);
+    // resident race CTAs of the whole GPU (queried once per device)
+    // the SM count and the race kernel's resident CTAs per SM, once per device
+    static std::atomic<int> s_sms[64], s_race_per_sm[64];
+    int dev = 0, sms = 0, race_per_sm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        sms = s_sms[dev].load(std::memory_order_relaxed);
+        race_per_sm = s_race_per_sm[dev].load(std::memory_order_relaxed);
+        if (!sms || !race_per_sm) {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&race_per_sm, va::decide_kernel, va::kRaceThreads, 0) !=
+                cudaSuccess)
+                race_per_sm = 0;
+            s_sms[dev].store(sms, std::memory_order_relaxed);
+            s_race_per_sm[dev].store(race_per_sm, std::memory_order_relaxed);
+        }
+    }
+    cudaGetLastError();
+    // statistics: two 1024-thread CTAs per SM are resident
+    const long long rows = (long long)num_seqs * (T + 1);
+    const int cluster = rows <= va::kClusterMaxRows                               ? va::kClusterMax
+                        : (sms > 0 && rows * va::kClusterWide <= 2LL * sms) ? va::kClusterWide
+                                                                            : va::kClusterNarrow;
+    cudaError_t e = va::launch_cluster(va::stats_kernel, dim3(cluster, T + 1, num_seqs), cluster, s, p);
+    const int slots = sms * race_per_sm;  // race CTAs resident on the whole GPU (0 if unknown)
+    // A row of race CTAs per sequence: kRacePerThread vocabulary entries per
+    // thread, but no more CTAs than one wave of the whole GPU spread over the
+    // sequences (a greedy sequence's CTAs exit after the prefix match, so a
+    // wide row only costs launches there; a sampled one loops over its slice).
+    long long nrace = ((long long)vocab + va::kRaceThreads * va::kRacePerThread - 1) /
+                      (va::kRaceThreads * va::kRacePerThread);
+    if (slots > 0) nrace = std::min<long long>(nrace, std::max<long long>(1, slots / num_seqs));
+    nrace = std::min<long long>(va::kMaxRaceCtas, std::max<long long>(1, nrace));
+    if (e == cudaSuccess)
+        e = va::launch_pdl(va::decide_kernel, dim3((unsigned)nrace, num_seqs), dim3(va::kRaceThreads), 0, s, p);
     if (e != cudaSuccess) {
         va::note_cuda_error(e);
         return VA_ERR_CUDA;
