@@ -5,7 +5,8 @@
 // One thread-block cluster per sequence (1 to 8 CTAs, from the history
 // length bound): CTA r scans the r-th slice of the end positions.  The last
 // max_match tokens (reversed) sit in each CTA's shared memory; every thread
-// walks end positions e (coalesced 4-byte loads of x[e]), extends a match
+// walks end positions e (coalesced 4-byte loads of x[e], eight in flight per
+// thread), extends a match
 // backwards only when x[e] equals the last token, and keeps the best
 // (length, e) as one 64-bit key (length in the high word, so the maximum is
 // the longest match and, among equal lengths, the most recent end).  A block
@@ -25,6 +26,7 @@ constexpr int kThreads = 1024;
 constexpr int kMaxMatch = 32;
 constexpr int kMaxCluster = 8;          // portable cluster size
 constexpr int kTokensPerCta = 4096;     // history tokens per CTA of the cluster (up to kMaxCluster CTAs)
+constexpr int kUnroll = 8;              // end-token loads per thread in flight together
 
 struct DraftParams {
     const int32_t *tokens;
@@ -60,13 +62,26 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const DraftParams p) {
         // this CTA's slice of end positions [0, L - 2]
         const int n_end = max(L - 1, 0), per = (n_end + nct - 1) / nct;
         const int e_hi = min(n_end, (rank + 1) * per);
-        for (int e = rank * per + tid; e < e_hi; e += kThreads) {
-            if (x[e] != last) continue;
-            int l = 1;
-            while (l < lmax && e - l >= 0 && x[e - l] == suf[l]) ++l;
-            if (l >= p.min_match) {
-                const unsigned long long key = ((unsigned long long)l << 32) | (unsigned)e;
-                best = key > best ? key : best;
+        // kUnroll coalesced loads of end tokens per thread are issued before
+        // any is compared, so that a thread's scan is a few memory round
+        // trips instead of one per end position
+        for (int e0 = rank * per + tid; e0 < e_hi; e0 += kThreads * kUnroll) {
+            int32_t v[kUnroll];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int e = e0 + k * kThreads;
+                v[k] = e < e_hi ? x[e] : 0;
+            }
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int e = e0 + k * kThreads;
+                if (e >= e_hi || v[k] != last) continue;
+                int l = 1;
+                while (l < lmax && e - l >= 0 && x[e - l] == suf[l]) ++l;
+                if (l >= p.min_match) {
+                    const unsigned long long key = ((unsigned long long)l << 32) | (unsigned)e;
+                    best = key > best ? key : best;
+                }
             }
         }
     }
