@@ -89,11 +89,28 @@ __device__ __forceinline__ uint32_t philox_first_word(uint32_t c0, uint32_t c1, 
     return c0;
 }
 
-// U(b, t, i, k) in (0, 1): 24 bits of the first Philox word, centred.
-__device__ __forceinline__ float uniform01(const AcceptParams &p, int b, int t, int i, int k) {
-    const uint32_t w = philox_first_word((uint32_t)i, (uint32_t)t, (uint32_t)b, (uint32_t)k, (uint32_t)p.seed,
-                                         (uint32_t)(p.seed >> 32));
-    return ((float)(w >> 8) + 0.5f) * 5.9604644775390625e-8f;  // 2^-24
+// j = the top 24 bits of the first Philox word on counter (i, t, b, k); U(b, t, i, k) = (j + 0.5) / 2^24
+// = (2j + 1) / 2^25, a 25-bit odd numerator that binary32 holds exactly only below 2^24.
+__device__ __forceinline__ uint32_t uniform_bits(const AcceptParams &p, int b, int t, int i, int k) {
+    return philox_first_word((uint32_t)i, (uint32_t)t, (uint32_t)b, (uint32_t)k, (uint32_t)p.seed,
+                             (uint32_t)(p.seed >> 32)) >> 8;
+}
+
+// U in binary32 rounded toward zero: within one ulp of U and strictly inside (0, 1) (rounding to
+// nearest would give 1.0 for j = 2^24 - 1).
+__device__ __forceinline__ float uniform01(uint32_t j) {
+    return __uint2float_rz(2u * j + 1u) * 2.98023223876953125e-8f;  // 2^-25
+}
+
+// -ln U to a few ulps for every j, also where U is within 2^-24 of 1 and -ln U is as small as
+// 2^-25: U = u_hi + u_lo with u_hi the nearest binary32 and u_lo = 0 or +-2^-25 (exact), and
+// ln U = ln u_hi + ln(1 + u_lo / u_hi), whose second term is u_lo / u_hi to within 2^-49.
+__device__ __forceinline__ float neg_log_uniform(uint32_t j) {
+    const uint32_t n = 2u * j + 1u;
+    const float nh = __uint2float_rn(n);
+    const float u_hi = nh * 2.98023223876953125e-8f;
+    const float u_lo = (float)(int)(n - __float2uint_rn(nh)) * 2.98023223876953125e-8f;
+    return -logf(u_hi) - __fdividef(u_lo, u_hi);
 }
 
 // Order-preserving map of a float to uint32 (larger float, larger code).
@@ -303,7 +320,7 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
     for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
         const bool valid = d[t] >= 0 && d[t] < p.V;
         const bool ok = greedy ? (valid && d[t] == st[t].argmax)
-                               : (valid && uniform01(p, b, t, 0, 0) * st[t].q_d < st[t].p_d);
+                               : (valid && uniform01(uniform_bits(p, b, t, 0, 0)) * st[t].q_d < st[t].p_d);
         if (!ok) atomicMin(&s_n, t);
     }
     __syncthreads();
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
     const int lo = min(p.V, (int)blockIdx.x * per), hi = min(p.V, lo + per);
     unsigned long long k = 0;
     for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-        const float g = -logf(-logf(uniform01(p, b, n, i, 1)));
+        const float g = -logf(neg_log_uniform(uniform_bits(p, b, n, i, 1)));
         float score;
         if (w) {
             const float r = expf(z[i] * inv - st[n].lse_p) - expf(w[i] * inv - st[n].lse_q);

@@ -95,3 +95,61 @@ def test_accept_argument_errors():
     with pytest.raises(ValueError):
         va.verify_attn_accept(torch.zeros((2, 3, 4), device="cuda"), torch.zeros((2, 3), dtype=torch.int32,
                               device="cuda"), torch.ones(2, device="cuda"), 1)
+
+
+def _one_hot_prefix(T, V, d_tok, rng):
+    """Positions 0..T-1 put logit 100 on the draft token (binary32 p(d) is
+    exactly 1, fp64 p(d) is 1 - V e^-100 = 1.0), so every draft is accepted
+    whenever u < 1; position T is a random row."""
+    z = np.zeros((1, T + 1, V), np.float32)
+    z[0, :T, d_tok] = 100.0
+    z[0, T] = rng.standard_normal(V).astype(np.float32)
+    return z, np.full((1, T), d_tok, np.int32), np.ones(1, np.float32)
+
+
+def test_accept_uniform_at_the_top_of_its_range():
+    # seed 46 draws j = 2^24 - 1 for the acceptance uniform of position 342,
+    # so U = 1 - 2^-25; its binary32 value must stay below 1 or the draft with
+    # p(d) = 1 would be rejected
+    seed, T, V = 46, 400, 8
+    assert sampler.uniform(seed, 0, 342, 0, 0) == 1.0 - 2.0 ** -25
+    z, d, tau = _one_hot_prefix(T, V, 3, np.random.default_rng(1))
+    out, n = run(z, d, tau, seed)
+    ref_out, ref_n, recs = sampler.accept(z, d, tau, seed, details=True)
+    assert ref_n[0] == T and n[0] == T
+    assert out[0, T] == ref_out[0, T] or near_tie(recs[0], int(n[0]), int(out[0, T]), int(ref_n[0]), tau[0])
+
+
+def test_race_gumbel_at_the_top_of_the_uniform_range():
+    # seed 2886 draws j = 2^24 - 1 for the race uniform of entry 1335 at
+    # position 2: its Gumbel is ln 2^25 = 17.33, finite, so with logit -30 it
+    # must lose to the zero-logit entries (an infinite Gumbel would win)
+    seed, T, V, i_top = 2886, 2, 4096, 1335
+    assert sampler.uniform(seed, 0, T, i_top, 1) == 1.0 - 2.0 ** -25
+    z, d, tau = _one_hot_prefix(T, V, 7, np.random.default_rng(2))
+    z[0, T] = 0.0
+    z[0, T, i_top] = -30.0
+    out, n = run(z, d, tau, seed)
+    ref_out, ref_n, recs = sampler.accept(z, d, tau, seed, details=True)
+    assert ref_n[0] == T and n[0] == T and ref_out[0, T] != i_top
+    assert out[0, T] != i_top
+    assert out[0, T] == ref_out[0, T] or near_tie(recs[0], int(n[0]), int(out[0, T]), int(ref_n[0]), tau[0])
+
+
+def test_race_gumbels_track_the_oracle_near_u_one():
+    # equal logits make the race a pure Gumbel maximum, decided among the
+    # largest uniforms, where -ln U is smallest (2^-25 at the top) and must
+    # be formed without rounding U to binary32 first: the winner must match
+    # the oracle's in every sequence (near ties excepted)
+    B, T, V = 32, 1, 50_000
+    rng = np.random.default_rng(4)
+    z = np.zeros((B, T + 1, V), np.float32)
+    z[:, 0, 5] = 100.0
+    d = np.full((B, T), 5, np.int32)
+    tau = np.ones(B, np.float32)
+    out, n = run(z, d, tau, 99)
+    ref_out, ref_n, recs = sampler.accept(z, d, tau, 99, details=True)
+    assert np.all(n == T) and np.all(ref_n == T)
+    bad = [b for b in range(B) if out[b, T] != ref_out[b, T]
+           and not near_tie(recs[b], int(n[b]), int(out[b, T]), int(ref_n[b]), tau[b])]
+    assert not bad, bad
