@@ -104,13 +104,14 @@ __device__ __forceinline__ float uniform01(uint32_t j) {
 
 // -ln U to a few ulps for every j, also where U is within 2^-24 of 1 and -ln U is as small as
 // 2^-25: U = u_hi + u_lo with u_hi the nearest binary32 and u_lo = 0 or +-2^-25 (exact), and
-// ln U = ln u_hi + ln(1 + u_lo / u_hi), whose second term is u_lo / u_hi to within 2^-49.
+// ln U = ln u_hi + ln(1 + u_lo / u_hi).  Below j = 2^23 the numerator 2j + 1 fits 24 bits and
+// u_lo = 0; above, it lies halfway between 2j and 2j + 2 and rounds to the even significand (2j
+// for even j, so u_lo = +2^-25; 2j + 2 for odd j, u_lo = -2^-25).  There u_hi is in [0.5, 1] and
+// u_lo (2 - u_hi) stands for u_lo / u_hi to within half an ulp of -ln U.
 __device__ __forceinline__ float neg_log_uniform(uint32_t j) {
-    const uint32_t n = 2u * j + 1u;
-    const float nh = __uint2float_rn(n);
-    const float u_hi = nh * 2.98023223876953125e-8f;
-    const float u_lo = (float)(int)(n - __float2uint_rn(nh)) * 2.98023223876953125e-8f;
-    return -logf(u_hi) - __fdividef(u_lo, u_hi);
+    const float u_hi = __uint2float_rn(2u * j + 1u) * 2.98023223876953125e-8f;  // 2^-25
+    const float u_lo = j < (1u << 23) ? 0.f : ((j & 1u) ? -2.98023223876953125e-8f : 2.98023223876953125e-8f);
+    return -logf(u_hi) - u_lo * (2.f - u_hi);
 }
 
 // Order-preserving map of a float to uint32 (larger float, larger code).
@@ -123,9 +124,10 @@ __device__ __forceinline__ float unordered(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// key = (ordered value, smallest index wins ties)
+// key = (ordered value, smallest index wins ties); -0 is keyed as +0, so that
+// equal values tie whatever their sign
 __device__ __forceinline__ unsigned long long vkey(float v, int i) {
-    return ((unsigned long long)ordered(v) << 32) | (0xFFFFFFFFu - (uint32_t)i);
+    return ((unsigned long long)ordered(v + 0.f) << 32) | (0xFFFFFFFFu - (uint32_t)i);
 }
 
 __device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long *red) {
@@ -231,6 +233,36 @@ __device__ __forceinline__ void row_pass(const float *row, int lo, int hi, bool 
     }
 }
 
+// Folds N scaled values (value k at vocabulary index index(k), increasing in
+// k) into a thread's running maximum m, its first index mi and the sum s of
+// exp(v - m): the round's maximum first; if it beats m, its first position
+// in the round and one rescale of s; then the round's exponentials (two
+// partial sums).
+template <int N, typename I>
+__device__ __forceinline__ void fold_round(float &m, int &mi, float &s, const float (&v)[N], I index) {
+    float rm = v[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k) rm = fmaxf(rm, v[k]);
+    if (rm > m) {
+        int ri = 0;
+#pragma unroll
+        for (int k = N - 1; k >= 0; --k)
+            if (v[k] == rm) ri = index(k);
+        s *= expf(m - rm);  // 0 while m is still -inf
+        m = rm;
+        mi = ri;
+    }
+    if (m > -INFINITY) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < N; k += 2) {
+            a0 += expf(v[k] - m);
+            if (k + 1 < N) a1 += expf(v[k + 1] - m);
+        }
+        s += a0 + a1;
+    }
+}
+
 // Row statistics over the cluster: max (and its smallest index) of row * scale,
 // and the log-sum-exp of row * scale when want_lse.
 __device__ void row_stats(const float *row, int V, float scale, bool want_lse, unsigned long long *redk,
@@ -241,15 +273,48 @@ __device__ void row_stats(const float *row, int V, float scale, bool want_lse, u
     // per thread: the largest value and its first index (a thread visits its
     // indices in increasing order, so a strict compare keeps the smallest
     // index of a tie); the 64-bit (value, index) key is formed once per thread
-    float tmax = -INFINITY;
+    float tmax = -INFINITY, tsum = 0.f;
     int tidx = -1;
-    row_pass(row, lo, hi, vec, [&](int i, float x) {
-        const float v = x * scale;
-        if (v > tmax) {
-            tmax = v;
-            tidx = i;
+    if (!want_lse) {
+        row_pass(row, lo, hi, vec, [&](int i, float x) {
+            const float v = x * scale;
+            if (v > tmax) {
+                tmax = v;
+                tidx = i;
+            }
+        });
+    } else if (vec) {
+        // one read of the row: the running sum of exp(v - running max),
+        // rescaled at most once per round of kVec 16-byte loads
+        const int step = (int)blockDim.x;
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        const int hi4 = hi >> 2;
+        int j = (lo >> 2) + (int)threadIdx.x;
+        for (; j + (kVec - 1) * step < hi4; j += kVec * step) {
+            float4 x[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) x[u] = __ldg(r4 + j + u * step);
+            float v[4 * kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                v[4 * u] = x[u].x * scale;
+                v[4 * u + 1] = x[u].y * scale;
+                v[4 * u + 2] = x[u].z * scale;
+                v[4 * u + 3] = x[u].w * scale;
+            }
+            fold_round(tmax, tidx, tsum, v, [&](int k) { return 4 * (j + (k >> 2) * step) + (k & 3); });
         }
-    });
+        for (; j < hi4; j += step) {
+            const float4 x = __ldg(r4 + j);
+            const float v[4] = {x.x * scale, x.y * scale, x.z * scale, x.w * scale};
+            fold_round(tmax, tidx, tsum, v, [&](int k) { return 4 * j + k; });
+        }
+    } else {
+        for (int i = lo + (int)threadIdx.x; i < hi; i += (int)blockDim.x) {
+            const float v[1] = {row[i] * scale};
+            fold_round(tmax, tidx, tsum, v, [&](int) { return i; });
+        }
+    }
     unsigned long long k = 0;
     if (tidx >= 0) {
         k = vkey(tmax, tidx);
@@ -261,10 +326,10 @@ __device__ void row_stats(const float *row, int V, float scale, bool want_lse, u
     argmax = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
     if (!want_lse) return;
     const float m = unordered((uint32_t)(k >> 32));
-    float s = 0.f;
-    row_pass(row, lo, hi, vec, [&](int, float x) { s += expf(x * scale - m); });
-    s = cluster_sum(block_sum(s, redf), slot_f);
-    lse = m + logf(s);
+    // this thread's sum moved from its own maximum to the row's (tmax <= m)
+    float sum = tidx >= 0 ? tsum * expf(tmax - m) : 0.f;
+    sum = cluster_sum(block_sum(sum, redf), slot_f);
+    lse = m + logf(sum);
 }
 
 __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const AcceptParams p) {
