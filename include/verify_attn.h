@@ -374,9 +374,10 @@ int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int3
  *     an exponential race); if every draft is accepted the bonus token is
  *     argmax_i [z[T][i] / tau + G_i] (a sample of p_T).  G_i = -ln(-ln
  *     U(b, t, i, 1)) are Gumbel variates of the emitting position t.
- *   U(b, t, i, k) = (floor(w / 2^8) + 0.5) / 2^24 with w the first word of
- *     Philox4x32-10 (Salmon et al., SC'11) on counter (i, t, b, k) and key
- *     (seed low word, seed high word): uniform in (0, 1), reproducible.
+ *   U(b, t, i, k) = (floor(w / 2^8) + 0.5) / 2^24 with w word number
+ *     (i mod 4) of Philox4x32-10 (Salmon et al., SC'11) on counter
+ *     (floor(i / 4), t, b, k) and key (seed low word, seed high word):
+ *     uniform in (0, 1), reproducible, one Philox call per four entries.
  * Outputs: out_tokens[b, 0 .. n-1] = d[0 .. n-1], out_tokens[b, n] = the
  * emitted token, -1 after it; num_accepted[b] = n (0 .. T).
  * Layouts (device): target_logits fp32 [num_seqs, T + 1, vocab];

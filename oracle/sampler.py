@@ -19,10 +19,12 @@ applied once ("DFlash2 drafting").  The rule, step by step:
     sample of the residual max(0, p_t - q_t) (normalised), else the bonus: a
     sample of p_T.  Samples are exponential races: argmax_i ln r_i + G_i with
     Gumbel variates G_i = -ln(-ln U_i).
-  U(b, t, i, k): the first word w of Philox4x32-10 (Salmon, Moraes, Dror and
-    Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11) on counter
-    (i, t, b, k) and key (seed low, seed high 32 bits), mapped to
-    (floor(w / 2^8) + 0.5) / 2^24.
+  U(b, t, i, k): word number (i mod 4) of the four that Philox4x32-10
+    (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2,
+    3", SC'11) gives for counter (floor(i / 4), t, b, k) and key (seed low,
+    seed high 32 bits), mapped to (floor(w / 2^8) + 0.5) / 2^24: one Philox
+    call serves four consecutive vocabulary entries.  (The pages fix no
+    random-number generator; this mapping is a reading.)
 """
 from __future__ import annotations
 
@@ -48,7 +50,10 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def uniform(seed: int, b: int, t: int, i, k: int):
-    w = philox4x32_10(i, t, b, k, seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)[0]
+    """U(b, t, i, k) for a scalar or an array of vocabulary indices i."""
+    i = np.asarray(i, np.uint64)
+    words = philox4x32_10(i // np.uint64(4), t, b, k, seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    w = np.choose((i % np.uint64(4)).astype(np.int64), words)
     return ((w >> np.uint32(8)).astype(np.float64) + 0.5) / 2.0 ** 24
 
 

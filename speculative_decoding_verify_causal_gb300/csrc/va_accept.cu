@@ -71,9 +71,10 @@ struct AcceptParams {
 };
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32
-// multiplies, the key bumped by the Weyl constants between rounds.
-__device__ __forceinline__ uint32_t philox_first_word(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                      uint32_t k0, uint32_t k1) {
+// multiplies, the key bumped by the Weyl constants between rounds; all four
+// output words (the compiler drops what a caller does not use).
+__device__ __forceinline__ uint4 philox4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                         uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
@@ -86,14 +87,16 @@ __device__ __forceinline__ uint32_t philox_first_word(uint32_t c0, uint32_t c1, 
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
-    return c0;
+    return make_uint4(c0, c1, c2, c3);
 }
 
-// j = the top 24 bits of the first Philox word on counter (i, t, b, k); U(b, t, i, k) = (j + 0.5) / 2^24
-// = (2j + 1) / 2^25, a 25-bit odd numerator that binary32 holds exactly only below 2^24.
-__device__ __forceinline__ uint32_t uniform_bits(const AcceptParams &p, int b, int t, int i, int k) {
-    return philox_first_word((uint32_t)i, (uint32_t)t, (uint32_t)b, (uint32_t)k, (uint32_t)p.seed,
-                             (uint32_t)(p.seed >> 32)) >> 8;
+// U(b, t, i, k) = (j + 0.5) / 2^24 = (2j + 1) / 2^25, j the top 24 bits of word (i mod 4) of Philox
+// on counter (i / 4, t, b, k): one Philox call serves four consecutive vocabulary entries.  The
+// 25-bit odd numerator is exact in binary32 only below 2^24.
+__device__ __forceinline__ uint4 uniform_bits4(const AcceptParams &p, int b, int t, int c, int k) {
+    const uint4 w = philox4((uint32_t)c, (uint32_t)t, (uint32_t)b, (uint32_t)k, (uint32_t)p.seed,
+                            (uint32_t)(p.seed >> 32));
+    return make_uint4(w.x >> 8, w.y >> 8, w.z >> 8, w.w >> 8);
 }
 
 // U in binary32 rounded toward zero: within one ulp of U and strictly inside (0, 1) (rounding to
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
     for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
         const bool valid = d[t] >= 0 && d[t] < p.V;
         const bool ok = greedy ? (valid && d[t] == st[t].argmax)
-                               : (valid && uniform01(uniform_bits(p, b, t, 0, 0)) * st[t].q_d < st[t].p_d);
+                               : (valid && uniform01(uniform_bits4(p, b, t, 0, 0).x) * st[t].q_d < st[t].p_d);
         if (!ok) atomicMin(&s_n, t);
     }
     __syncthreads();
@@ -394,26 +397,55 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
         if (blockIdx.x == 0) write_tokens(p, b, n, st[n].argmax);
         return;
     }
-    // the race: this CTA's slice of the vocabulary
+    // the race: this CTA's slice of the vocabulary, in groups of four
+    // entries that share one Philox counter (16-byte loads of the logits
+    // where the rows allow)
     const float inv = 1.f / tau;
     const float *z = p.z + ((size_t)b * (p.T + 1) + n) * p.V;
     const bool bonus = n == p.T;
     const int dn = bonus ? -1 : d[n];
     const float *w = (!bonus && p.w) ? p.w + ((size_t)b * p.T + n) * p.V : nullptr;
-    const int per = (p.V + (int)gridDim.x - 1) / (int)gridDim.x;
-    const int lo = min(p.V, (int)blockIdx.x * per), hi = min(p.V, lo + per);
+    const bool vec = (p.V & 3) == 0 && (reinterpret_cast<uintptr_t>(z) & 15u) == 0 &&
+                     (!w || (reinterpret_cast<uintptr_t>(w) & 15u) == 0);
+    const float lse_p = st[n].lse_p, lse_q = st[n].lse_q;
+    const int groups = (p.V + 3) >> 2;
+    const int per = (groups + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int lo = min(groups, (int)blockIdx.x * per), hi = min(groups, lo + per);
     unsigned long long k = 0;
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-        const float g = -logf(neg_log_uniform(uniform_bits(p, b, n, i, 1)));
-        float score;
-        if (w) {
-            const float r = expf(z[i] * inv - st[n].lse_p) - expf(w[i] * inv - st[n].lse_q);
-            score = r > 0.f ? logf(r) + g : -INFINITY;
+    for (int c = lo + (int)threadIdx.x; c < hi; c += blockDim.x) {
+        const uint4 j4 = uniform_bits4(p, b, n, c, 1);
+        const uint32_t js[4] = {j4.x, j4.y, j4.z, j4.w};
+        const int i0 = 4 * c;
+        float zv[4], wv[4];
+        if (vec) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(z) + c);
+            zv[0] = a.x, zv[1] = a.y, zv[2] = a.z, zv[3] = a.w;
+            if (w) {
+                const float4 e = __ldg(reinterpret_cast<const float4 *>(w) + c);
+                wv[0] = e.x, wv[1] = e.y, wv[2] = e.z, wv[3] = e.w;
+            }
         } else {
-            score = i == dn ? -INFINITY : z[i] * inv + g;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                zv[e] = i0 + e < p.V ? z[i0 + e] : 0.f;
+                if (w) wv[e] = i0 + e < p.V ? w[i0 + e] : 0.f;
+            }
         }
-        const unsigned long long c = vkey(score, i);
-        k = c > k ? c : k;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = i0 + e;
+            if (i >= p.V) break;
+            const float g = -logf(neg_log_uniform(js[e]));
+            float score;
+            if (w) {
+                const float r = expf(zv[e] * inv - lse_p) - expf(wv[e] * inv - lse_q);
+                score = r > 0.f ? logf(r) + g : -INFINITY;
+            } else {
+                score = i == dn ? -INFINITY : zv[e] * inv + g;
+            }
+            const unsigned long long key = vkey(score, i);
+            k = key > k ? key : k;
+        }
     }
     k = block_max_u64(k, redk);
     SeqSlot *slot = p.slots + b;

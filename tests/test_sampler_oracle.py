@@ -27,6 +27,26 @@ def test_uniform_is_open_unit_interval_and_flat():
     assert np.all(np.abs(hist - 10000) < 600)
 
 
+def test_uniform_words_of_one_counter_are_flat_and_uncorrelated():
+    # four consecutive entries share a Philox counter, one word each: every
+    # word position must be flat on its own, and neighbours (same counter or
+    # across counters) uncorrelated -- a wrong word choice (say the first
+    # word for all four) repeats values and fails both
+    n = 400_000
+    u = sampler.uniform(7, 3, 2, np.arange(n, dtype=np.uint64), 1)
+    # 24-bit values: about n^2 / 2^25 repeats by chance (4,800 here)
+    assert len(np.unique(u)) > n - 1.2 * n * n / 2 ** 25
+    for r in range(4):
+        hist = np.histogram(u[r::4], bins=10, range=(0, 1))[0]
+        assert np.all(np.abs(hist - n / 40) < 0.06 * n / 40)
+    for lag in (1, 2, 3, 4):
+        c = np.corrcoef(u[:-lag], u[lag:])[0, 1]
+        assert abs(c) < 0.01
+    # entry 0 of every position is word 0 of counter (0, t, b, k)
+    w0 = sampler.philox4x32_10(0, 2, 3, 1, 7, 0)[0]
+    assert u[0] == ((int(w0) >> 8) + 0.5) / 2 ** 24
+
+
 def test_greedy_prefix_rule():
     rng = np.random.default_rng(1)
     B, T, V = 50, 6, 9
