@@ -389,7 +389,8 @@ int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int3
  * share one workspace must be ordered on one stream.  The decisions are taken in binary32 (the scores,
  * exponentials and logarithms of the CUDA math library; u_t is U rounded toward zero, so below 1,
  * and each Gumbel takes -ln U to a few ulps from the exact U, whose nearest binary32 value can be
- * 1 or lose the low bit that decides -ln U near 1), so a CPU restatement
+ * 1 or lose the low bit that decides -ln U near 1; the race ranks scores in units of ln 2, with
+ * the hardware base-2 logarithm (absolute error about 1e-6) for ln(-ln U) and ln r), so a CPU restatement
  * in another precision agrees except where two scores, or u and p/q, are
  * within a few ulps.  Returns VA_OK when enqueued, VA_ERR_INVALID_ARGUMENT
  * for bad arguments (T >= 1, vocab >= 1, draft tokens outside [0, vocab) are

@@ -399,7 +399,9 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
     }
     // the race: this CTA's slice of the vocabulary, in groups of four
     // entries that share one Philox counter (16-byte loads of the logits
-    // where the rows allow)
+    // where the rows allow); scores in units of ln 2, the outer logarithm
+    // of the Gumbel and ln r taken by the hardware base-2 logarithm
+    // (absolute error about 1e-6, far below any race margin that matters)
     const float inv = 1.f / tau;
     const float *z = p.z + ((size_t)b * (p.T + 1) + n) * p.V;
     const bool bonus = n == p.T;
@@ -435,13 +437,13 @@ __global__ void __launch_bounds__(kRaceThreads) decide_kernel(const AcceptParams
         for (int e = 0; e < 4; ++e) {
             const int i = i0 + e;
             if (i >= p.V) break;
-            const float g = -logf(neg_log_uniform(js[e]));
-            float score;
+            const float g2 = -__log2f(neg_log_uniform(js[e]));  // Gumbel / ln 2
+            float score;  // in units of ln 2
             if (w) {
                 const float r = expf(zv[e] * inv - lse_p) - expf(wv[e] * inv - lse_q);
-                score = r > 0.f ? logf(r) + g : -INFINITY;
+                score = r > 0.f ? __log2f(r) + g2 : -INFINITY;
             } else {
-                score = i == dn ? -INFINITY : zv[e] * inv + g;
+                score = i == dn ? -INFINITY : fmaf(zv[e], inv * 1.4426950408889634f, g2);
             }
             const unsigned long long key = vkey(score, i);
             k = key > k ? key : k;
