@@ -54,12 +54,11 @@ def near_tie(rec, n_gpu, tok_gpu, n_ref, tau_b):
     return False
 
 
-@pytest.mark.parametrize("B,T,V,model", [(64, 5, 50, False), (32, 16, 1000, False), (16, 8, 32000, False),
-                                         (32, 5, 1000, True), (4, 16, 151_936, False)])
-def test_accept_matches_oracle(B, T, V, model):
-    z, d, tau, w = make(B * 7 + T + V, B, T, V, model=model)
-    seed = 0x1234_5678_9ABC + V
-    out, n = run(z, d, tau, seed, w)
+def check_against_oracle(z, d, tau, seed, w, out, n):
+    """Greedy rows exact; sampled rows equal or at a genuine near-tie, and
+    such rows rare; every row well formed."""
+    B, T = d.shape
+    V = z.shape[2]
     ref_out, ref_n, recs = sampler.accept(z, d, tau, seed, draft_logits=w, details=True)
     mism = 0
     for b in range(B):
@@ -74,6 +73,40 @@ def test_accept_matches_oracle(B, T, V, model):
     for b in range(B):
         assert np.array_equal(out[b, :n[b]], d[b, :n[b]]) and 0 <= out[b, n[b]] < V
         assert np.all(out[b, n[b] + 1:] == -1)
+
+
+@pytest.mark.parametrize("B,T,V,model", [(64, 5, 50, False), (32, 16, 1000, False), (16, 8, 32000, False),
+                                         (32, 5, 1000, True), (4, 16, 151_936, False), (64, 5, 151_936, False),
+                                         (8, 4, 777, True), (6, 3, 50, True)])
+def test_accept_matches_oracle(B, T, V, model):
+    # the last three: the benchmark's batch of 64 sequences over the full
+    # vocabulary (race grid capped at one GPU wave), and model drafters on
+    # vocabularies that are not a multiple of 4 (scalar loads in both kernels)
+    z, d, tau, w = make(B * 7 + T + V, B, T, V, model=model)
+    seed = 0x1234_5678_9ABC + V
+    out, n = run(z, d, tau, seed, w)
+    check_against_oracle(z, d, tau, seed, w, out, n)
+
+
+def test_accept_logits_off_a_16_byte_boundary():
+    # V a multiple of 4, but both logit arrays start 4 bytes past a 16-byte
+    # boundary: both kernels must take their scalar loads
+    import speculative_decoding_verify_causal_gb300 as va
+    B, T, V = 16, 4, 1000
+    z, d, tau, w = make(77, B, T, V, model=True)
+
+    def shifted(a):
+        buf = torch.empty(a.size + 1, dtype=torch.float32, device="cuda")
+        t = buf[1:].view(a.shape)
+        t.copy_(torch.from_numpy(a))
+        assert t.data_ptr() % 16 == 4
+        return t
+
+    seed = 4242
+    out, n = va.verify_attn_accept(shifted(z), torch.from_numpy(d).cuda(), torch.from_numpy(tau).cuda(), seed,
+                                   shifted(w))
+    torch.cuda.synchronize()
+    check_against_oracle(z, d, tau, seed, w, out.cpu().numpy(), n.cpu().numpy())
 
 
 def test_accept_all_greedy_exact_and_bonus():
