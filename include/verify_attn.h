@@ -346,9 +346,10 @@ int verify_attn_kv_append(const void *k_new, const void *v_new, int num_seqs, in
  * num_draft]; draft_len, match_end, match_len int32 [num_seqs].  Limits:
  * 1 <= min_match <= max_match <= 32, 1 <= num_draft <= 256.  Returns VA_OK
  * when enqueued, VA_ERR_INVALID_ARGUMENT otherwise, VA_ERR_CUDA if the launch
- * fails.  One thread-block cluster of 1 to 8 CTAs scans each sequence (one
- * CTA per 4,096 tokens of token_stride, at most 8), the CTAs' best matches
- * combined through distributed shared memory. */
+ * fails.  One thread-block cluster scans each sequence: one CTA per 4,096
+ * tokens of token_stride, at most 16 where the device can place a cluster of
+ * that (non-portable) size and 8 otherwise, the CTAs' best matches combined
+ * through distributed shared memory. */
 int verify_attn_lookup_draft(const int32_t *tokens, int token_stride, const int32_t *lens,
                              int num_seqs, int min_match, int max_match, int num_draft,
                              int32_t *draft, int32_t *draft_len, int32_t *match_end,

@@ -2,8 +2,9 @@
 // request on a RTX 3090", "Lookup-augmented drafting"): find the most recent
 // earlier occurrence of the history's last tokens and propose what followed.
 //
-// One thread-block cluster per sequence (1 to 8 CTAs, from the history
-// length bound): CTA r scans the r-th slice of the end positions.  The last
+// One thread-block cluster per sequence (1 to 16 CTAs, from the history
+// length bound; above 8, a non-portable size, used where the device can place
+// it): CTA r scans the r-th slice of the end positions.  The last
 // max_match tokens (reversed) sit in each CTA's shared memory; every thread
 // walks end positions e (coalesced 4-byte loads of x[e], eight in flight per
 // thread), extends a match
@@ -13,6 +14,7 @@
 // max-reduction, then CTA 0 reads the other CTAs' keys through distributed
 // shared memory and its first num_draft threads copy the continuation.
 #include <algorithm>
+#include <atomic>
 
 #include "va_internal.h"
 #include "va_sm100.cuh"
@@ -24,8 +26,8 @@ using namespace sm100;
 
 constexpr int kThreads = 1024;
 constexpr int kMaxMatch = 32;
-constexpr int kMaxCluster = 8;          // portable cluster size
-constexpr int kTokensPerCta = 4096;     // history tokens per CTA of the cluster (up to kMaxCluster CTAs)
+constexpr int kMaxCluster = 8;          // portable cluster size (twice that where allowed)
+constexpr int kTokensPerCta = 4096;     // history tokens per CTA of the cluster
 constexpr int kUnroll = 8;              // end-token loads per thread in flight together
 
 struct DraftParams {
@@ -134,8 +136,34 @@ extern "C" int verify_attn_lookup_draft(const int32_t *tokens, int token_stride,
     p.min_match = min_match;
     p.max_match = max_match;
     p.num_draft = num_draft;
-    // cluster of CTAs per sequence: one per kTokensPerCta of the longest possible history
-    const int nct = std::min(va::kMaxCluster, std::max(1, (token_stride + va::kTokensPerCta - 1) / va::kTokensPerCta));
+    // cluster of CTAs per sequence: one per kTokensPerCta of the longest possible history,
+    // up to 16 (a non-portable size, refused on parts that cannot place it: then 8)
+    static std::atomic<int> s_wide{0};  // 0 unknown, 1 allowed, -1 refused
+    int wide = s_wide.load(std::memory_order_relaxed);
+    if (wide == 0) {
+        // allowed, and at least one such cluster fits on the device
+        wide = -1;
+        if (cudaFuncSetAttribute(va::lookup_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(2 * va::kMaxCluster, 1);
+            q.blockDim = dim3(va::kThreads);
+            cudaLaunchAttribute ca;
+            ca.id = cudaLaunchAttributeClusterDimension;
+            ca.val.clusterDim.x = 2 * va::kMaxCluster;
+            ca.val.clusterDim.y = 1;
+            ca.val.clusterDim.z = 1;
+            q.attrs = &ca;
+            q.numAttrs = 1;
+            int nclusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, va::lookup_kernel, &q) == cudaSuccess && nclusters >= 1)
+                wide = 1;
+        }
+        (void)cudaGetLastError();
+        s_wide.store(wide, std::memory_order_relaxed);
+    }
+    const int cap = wide > 0 ? 2 * va::kMaxCluster : va::kMaxCluster;
+    int nct = std::min(cap, std::max(1, (token_stride + va::kTokensPerCta - 1) / va::kTokensPerCta));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nct, num_seqs);
     cfg.blockDim = dim3(va::kThreads);
@@ -149,7 +177,15 @@ extern "C" int verify_attn_lookup_draft(const int32_t *tokens, int token_stride,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, va::lookup_kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, va::lookup_kernel, p);
+    if (e != cudaSuccess && nct > va::kMaxCluster) {  // the wide cluster was refused: portable size
+        (void)cudaGetLastError();
+        s_wide.store(-1, std::memory_order_relaxed);
+        nct = va::kMaxCluster;
+        cfg.gridDim = dim3(nct, num_seqs);
+        attr[0].val.clusterDim.x = nct;
+        e = cudaLaunchKernelEx(&cfg, va::lookup_kernel, p);
+    }
     if (e != cudaSuccess) {
         va::note_cuda_error(e);
         return VA_ERR_CUDA;
