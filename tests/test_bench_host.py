@@ -32,3 +32,32 @@ def test_cpu_baseline_line_on_the_small_workload():
 def test_cpu_model_is_a_nonempty_string():
     m = bench.cpu_model()
     assert isinstance(m, str) and len(m) > 0
+
+
+def test_reference_arm_prints_one_contract_line():
+    # `bench.py --impl reference` times the fp64 oracle on the host cores and
+    # prints one JSON line with the reference-arm keys (CPU only)
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
+
+
+def test_default_run_keeps_the_warmup_rule():
+    # the driver's default invocation: at least 3 untimed warm-up steps
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        a = bench.parse_args()
+    finally:
+        sys.argv = old
+    assert a.warmup >= 3 and a.steps >= 1 and a.gpus == 1 and a.impl == "ours" and a.config == "lookup16"
